@@ -1,0 +1,476 @@
+"""Throughput of the per-shard mixed-precision ZeRO optimizer step on GB300.
+
+Default workload: a GPT-2-small-sized flat buffer of 124,439,808 parameters,
+N = 1 (unsharded, DDP-equivalent), bf16 gradients ~N(0, 1e-2), AdamW lr 3e-4
+wd 0.01, global L2 clip 1.0, no loss scaling.  Inputs are synthetic and seeded
+and are resident in HBM before the timed region; they are larger than L2
+(3.5 GB of algorithmic traffic per step), so no L2 flush is needed.
+
+One "step" is one call of zero_opt_step: pass 1 (reduce, overflow flag, sum of
+squares, decision) and pass 2 (unscale, clip, AdamW, 16-bit copy).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload gpt2|llama|fused|pertensor]
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own copy of
+the workload on its own GPU (weak scaling) and the timing is the maximum over
+ranks.  --impl reference times the CPU oracle (single-threaded C++) on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "optimizer-step params/s and achieved HBM GB/s (% of GB300 peak), 1 GPU"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------- workloads
+
+def llama_shapes():
+    H, KV, F, V = 4096, 1024, 14336, 128256
+    shapes = [(V, H)]
+    for _ in range(8):
+        shapes += [(H, H), (KV, H), (KV, H), (H, H), (F, H), (F, H), (H, F), (H,), (H,)]
+    return shapes
+
+
+WORKLOADS = {
+    "gpt2": dict(desc="GPT-2-small-sized flat buffer, 124,439,808 params, N=1, bf16 grads "
+                      "~N(0,1e-2), AdamW lr 3e-4 wd 0.01, global L2 clip 1.0, no loss scaling",
+                 numel=124_439_808, world=1, R=1, K=1, dtype="bf16", lr=3e-4, wd=0.01,
+                 clip=1.0, dynamic=False, scale=1.0, sigma=1e-2, seed=0x5EED0002),
+    "llama": dict(desc="Llama-3-8B ZeRO-2 shard: rank 0 of N=8 over 8,030,261,248 params "
+                       "(1,003,782,656-param shard), fp16 grads ~N(0,1e-4) x dynamic scale 2^16, "
+                       "window 1000, AdamW lr 1e-4 wd 0.1",
+                  numel=8_030_261_248, world=8, R=1, K=1, dtype="fp16", lr=1e-4, wd=0.1,
+                  clip=0.0, dynamic=True, scale=65536.0, sigma=1e-4, seed=0x5EED0003),
+    "fused": dict(desc="fused local rank reduction + step: 250,000,000-param shard, 8 ranks x "
+                       "4 micro-steps of fp16 grads ~N(0,1e-3) x 1024, divided by 32, AdamW lr "
+                       "2e-4 wd 0.01, clip 1.0",
+                  numel=250_000_000, world=1, R=8, K=4, dtype="fp16", lr=2e-4, wd=0.01,
+                  clip=1.0, dynamic=False, scale=1024.0, sigma=1e-3, seed=0x5EED0004),
+    "pertensor": dict(desc="per-tensor list: Llama-3-8B embedding + 8 decoder layers, 73 "
+                           "tensors, 2,270,232,576 params, bf16 grads ~N(0,1e-3), AdamW lr 1e-4 "
+                           "wd 0.1, clip 1.0",
+                      numel=2_270_232_576, world=1, R=1, K=1, dtype="bf16", lr=1e-4, wd=0.1,
+                      clip=1.0, dynamic=False, scale=1.0, sigma=1e-3, seed=0x5EED0005),
+}
+
+
+def algorithmic_bytes_per_param(w):
+    # R*K 16-bit gradient reads + 12 B fp32 master/m/v read + 12 B written + 2 B 16-bit copy
+    return 2 * w["R"] * w["K"] + 12 + 12 + 2
+
+
+def pass2_bytes_per_param(w, stash):
+    # pass 2 alone: gradients (or the fp32 stash) read, state read and written, copy written
+    return (4 if stash else 2 * w["R"] * w["K"]) + 26
+
+
+class Setup:
+    """Device buffers of one workload, filled by the seeded generator."""
+
+    def __init__(self, name, device):
+        import torch
+
+        import synth
+        import zero_sharded_mixed_05_gb300 as z
+        w = WORKLOADS[name]
+        self.w, self.name, self.z = w, name, z
+        code = z.FP16 if w["dtype"] == "fp16" else z.BF16
+        tdt = torch.float16 if code == z.FP16 else torch.bfloat16
+        kind = synth.F16 if code == z.FP16 else synth.BF16
+        self.tdt = tdt
+        cfg = z.make_config(numel=w["numel"], world=w["world"], grad_dtype=code, lr=w["lr"],
+                            weight_decay=w["wd"], max_grad_norm=w["clip"],
+                            dynamic_scale=w["dynamic"], init_scale=w["scale"],
+                            scale_window=1000)
+        self.h = z.zero_opt_create(cfg)
+        nb = w["R"] * w["K"]
+        self.stash = None
+        if name == "pertensor":
+            shapes = llama_shapes()
+            self.items, off = [], 0
+            for shp in shapes:
+                n = int(np.prod(shp))
+                master = torch.empty(n, dtype=torch.float32, device=device)
+                synth.fill_gpu(master, w["seed"], 0, off, 0.02, synth.F32)
+                g = torch.empty(n, dtype=tdt, device=device)
+                synth.fill_gpu(g, w["seed"], 1, off, w["sigma"] * w["scale"], kind)
+                self.items.append(dict(numel=n, master=master,
+                                       m=torch.zeros(n, device=device),
+                                       v=torch.zeros(n, device=device),
+                                       param16=master.to(tdt), grads=[g]))
+                off += n
+            self.n = off
+            self.lst = z.make_tensor_list(self.items)
+            self.grads = [it["grads"][0] for it in self.items]
+            self.p16 = [it["param16"] for it in self.items]
+        else:
+            b, e, S, P = z.zero_opt_shard_bounds(self.h, 0)
+            self.n = e - b
+            n = self.n
+            self.master = torch.empty(n, dtype=torch.float32, device=device)
+            synth.fill_gpu(self.master, w["seed"], 0, b, 0.02, synth.F32)
+            self.m = torch.zeros(n, device=device)
+            self.v = torch.zeros(n, device=device)
+            # ZeRO-2 keeps the full 16-bit parameter buffer; the step writes its slice
+            self.p16_full = torch.zeros(P, dtype=tdt, device=device)
+            self.p16_full[b:e].copy_(self.master)
+            self.grads = []
+            for i in range(nb):
+                g = torch.empty(n, dtype=tdt, device=device)   # shard-local (reduce-scattered)
+                synth.fill_gpu(g, w["seed"], 1 + i, b, w["sigma"] * w["scale"], kind)
+                self.grads.append(g)
+            if nb > 4:
+                self.stash = torch.empty(n, dtype=torch.float32, device=device)
+            self.bufs = z.make_buffers(self.master, self.m, self.v, self.p16_full, self.grads,
+                                       n_ranks=w["R"], n_micro=w["K"], grads_shard_local=True,
+                                       stash=self.stash)
+            self.p16 = [self.p16_full[b:e]]
+        torch.cuda.synchronize()
+
+    def step(self, stream=None):
+        if self.name == "pertensor":
+            self.z.zero_opt_step_tensors(self.h, 0, self.lst, stream)
+        else:
+            self.z.zero_opt_step(self.h, 0, self.bufs, stream)
+
+    def input_bytes(self):
+        return sum(g.numel() * g.element_size() for g in self.grads)
+
+    def output_bytes(self):
+        return sum(p.numel() * p.element_size() for p in self.p16)
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.idx)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((ts, parts))
+        inside = [p for ts, p in rows if t0 - 0.15 <= ts <= t1 + 0.15] or [p for _, p in rows]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        mx = [num(p[2]) for p in inside if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4)
+                          if p[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside),
+                "power_w_max": max((num(p[3]) or 0.0) for p in inside)}
+
+
+# ---------------------------------------------------------------- arms
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class OracleSample:
+    """The single-threaded C++ oracle on a contiguous sample of the workload
+    (same generator, same hyper-parameters); inputs are generated once."""
+
+    def __init__(self, name, elems=4_000_000):
+        import oracle as O
+        import synth
+        w = WORKLOADS[name]
+        self.O = O
+        self.code = O.FP16 if w["dtype"] == "fp16" else O.BF16
+        kind = synth.F16 if self.code == O.FP16 else synth.BF16
+        self.nb = w["R"] * w["K"]
+        self.n = n = min(w["numel"] // w["world"], max(elems // self.nb, 1))
+        self.master = synth.normal_np(w["seed"], 0, 0, n, 0.02, synth.F32)
+        self.grads = [synth.normal_np(w["seed"], 1 + i, 0, n, w["sigma"] * w["scale"], kind)
+                      for i in range(self.nb)]
+        self.m = np.zeros(n, np.float32)
+        self.v = np.zeros(n, np.float32)
+        self.p16 = np.zeros(n, np.uint16)
+        self.hp = O.hparams(lr=w["lr"], weight_decay=w["wd"], max_grad_norm=w["clip"],
+                            dynamic_scale=w["dynamic"])
+        self.st = O.scaler(w["scale"])
+        self.total_steps = 0
+        self.total_s = 0.0
+
+    def rate(self, budget_s):
+        """Params/s over oracle steps run for about budget_s seconds."""
+        steps = 0
+        t0 = time.perf_counter()
+        while True:
+            self.O.step(self.hp, self.st, self.grads, self.code, self.master, self.m, self.v,
+                        self.p16, self.code, float(self.nb))
+            steps += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s:
+                break
+        self.total_steps += steps
+        self.total_s += el
+        return self.n * steps / el
+
+    def info(self):
+        return dict(kind="oracle", cores=1,
+                    sample=f"{self.total_steps} oracle steps over the first {self.n:,} "
+                           f"parameters of the workload ({self.nb} gradient buffer(s)), "
+                           f"{self.total_s:.1f} s of CPU time")
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    name = args.workload
+    sample = OracleSample(name)
+    for _ in range(args.warmup):
+        sample.rate(0.05)
+    sample.total_steps, sample.total_s = 0, 0.0
+    per_step = max(0.05, min(5.0, 60.0 / max(args.steps, 1)))
+    rates = [sample.rate(per_step) for _ in range(args.steps)]
+    value = statistics.median(rates)
+    w = WORKLOADS[name]
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "params/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * (w["numel"] // w["world"]) / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded SplitMix64 / Irwin-Hall)",
+            "config": {"workload": w["desc"], "params": w["numel"] // w["world"]},
+            "cpu_baseline": {"value": value, "unit": "params/s", **sample.info()},
+            "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def run_ours(args):
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    import __graft_entry__
+    if rank == 0 or ws == 1:
+        __graft_entry__.build()
+    if ws > 1:
+        torch.distributed.barrier()
+        __graft_entry__.build()
+    import zero_sharded_mixed_05_gb300 as z
+
+    setup = Setup(args.workload, dev)
+    w = setup.w
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    for _ in range(args.warmup):
+        setup.step(sp)
+    torch.cuda.synchronize()
+
+    # per-pass events on the launching stream, for every timed step
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    for trio in evs:
+        for e in trio:
+            e.record(stream)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    # keep the GPU busy while the sampler starts
+    t_spin = time.time()
+    while time.time() - t_spin < 0.3:
+        setup.step(sp)
+    launches0 = z.zero_opt_launch_count(setup.h)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    start.record(stream)
+    for i in range(K):
+        z.zero_opt_set_events(setup.h, *evs[i])
+        setup.step(sp)
+    end.record(stream)
+    z.zero_opt_set_events(setup.h)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    launches = z.zero_opt_launch_count(setup.h) - launches0
+    if ws > 1:
+        torch.distributed.barrier()
+    ms_total = start.elapsed_time(end)
+    # keep sampling a little after the region, then stop
+    clocks.stop()
+    clk = clocks.summary(t0, t1)
+    p1 = [evs[i][0].elapsed_time(evs[i][1]) for i in range(K)]
+    p2 = [evs[i][1].elapsed_time(evs[i][2]) for i in range(K)]
+    if ws > 1:
+        t = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / K
+    n = setup.n
+    value = ws * n / (ms_step * 1e-3)
+    peak, peak_src = load_peaks()
+    step_bytes = algorithmic_bytes_per_param(w) * n
+    stash = setup.stash is not None
+    p2_bytes = pass2_bytes_per_param(w, stash) * n
+    p2_ms = statistics.mean(p2)
+    p1_ms = statistics.mean(p1)
+    achieved = p2_bytes / (p2_ms * 1e-3) / 1e9
+    step_gbs = step_bytes / (ms_step * 1e-3) / 1e9
+
+    # end to end through the public API with host buffers: H2D of the step's
+    # gradients from pinned memory, the step, D2H of the 16-bit parameters
+    host_g = [torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in setup.grads]
+    for hg, g in zip(host_g, setup.grads):
+        hg.copy_(g)
+    host_p = [torch.empty(p.shape, dtype=p.dtype, pin_memory=True) for p in setup.p16]
+    Ke = max(3, min(K, 50))
+    for _ in range(2):
+        for hg, g in zip(host_g, setup.grads):
+            g.copy_(hg, non_blocking=True)
+        setup.step(sp)
+        for hp_, p in zip(host_p, setup.p16):
+            hp_.copy_(p, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(Ke):
+        for hg, g in zip(host_g, setup.grads):
+            g.copy_(hg, non_blocking=True)
+        setup.step(sp)
+        for hp_, p in zip(host_p, setup.p16):
+            hp_.copy_(p, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / Ke
+    if ws > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = ws * n / (e2e_ms * 1e-3)
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        sample = OracleSample(args.workload)
+        rate = sample.rate(args.cpu_seconds)
+        cpu = {"value": rate, "unit": "params/s", **sample.info()}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "params/s", "n_gpus": ws, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded SplitMix64 / Irwin-Hall), resident in HBM",
+            "config": {"workload": w["desc"], "params_per_gpu": n,
+                       "grad_dtype": w["dtype"], "grad_buffers": w["R"] * w["K"],
+                       "l2": "inputs larger than L2 (algorithmic %.2f GB per step)" % (step_bytes / 1e9),
+                       "stash": stash},
+            "hbm_gbs": step_gbs, "hbm_frac": step_gbs / peak,
+            "algorithmic_bytes_per_param": algorithmic_bytes_per_param(w),
+            "roofline": {"bound": "hbm", "kernel": "pass2_kernel (unscale+clip+AdamW+cast)",
+                         "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": peak_src + " (hbm_gbs)",
+                         "traffic": None, "bytes_per_launch": p2_bytes,
+                         "avg_launch_ms": p2_ms, "pass1_avg_ms": p1_ms},
+            "e2e": {"value": e2e_value, "unit": "params/s",
+                    "h2d_bytes_per_step": setup.input_bytes(),
+                    "d2h_bytes_per_step": setup.output_bytes(), "ms_per_step": e2e_ms},
+            "gpu_launches": launches,
+            "clocks": clk,
+        }
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line))
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gpt2")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,305 @@
+/*
+ * zero_opt.h -- C ABI of the GB300 per-shard mixed-precision ZeRO optimizer
+ * step.
+ *
+ * One call of zero_opt_step performs, for the shard a data-parallel rank owns,
+ * the whole optimizer step of a ZeRO training engine:
+ *   (i)   the local reduction of the simulated ranks' and accumulation
+ *         micro-steps' 16-bit gradients (the reduce half of reduce-scatter),
+ *   (ii)  unscaling by the dynamic loss scale,
+ *   (iii) overflow (inf/NaN) detection and the global L2 norm for clipping,
+ *   (iv)  the fp32 Adam/AdamW update of the master weights, m and v, and
+ *   (v)   the write-back of the 16-bit parameter copy,
+ * and advances the loss scale: halve and skip on overflow, double after
+ * scale_window clean steps.
+ *
+ * Sources (page title, section):
+ *   "DeepSpeed tutorial" (devpress.csdn.net): §2.1 the 16Ψ model-state bytes
+ *     and ZeRO-1/2/3; §2.2 loss scaling (scale the loss, unscale before the
+ *     update, lower on overflow, raise when stable); §2.3 gradient
+ *     accumulation; §2.4 each GPU's optimizer updates only its own slice;
+ *     §3.2 ds_config.json (AdamW lr/betas/eps/weight_decay, fp16
+ *     loss_scale_window / initial_scale_power / hysteresis / min_loss_scale).
+ *   "DeepSpeed ZeRO引擎深入" (aiqz.cc): "显存四巨头" (2 + 2 + 12 bytes per
+ *     parameter), "ZeRO三阶段" (cut the state into N parts), "混合精度"
+ *     (update on the fp32 master copy), "Python 演示" (Adam moments, eps in
+ *     the denominator).
+ *   "LLM-train tutorials ch01" (jwzheng96.github.io): §1.2 M_DDP and
+ *     M_ZeRO-1/2/3 equations; stage table (reduce-scatter / all-gather).
+ *   "DeepSpeed framework interview answer" (algomooc.com): "ZeRO 三阶段"
+ *     (reduce-scatter gradients, update local shard, all-gather parameters).
+ *
+ * Conventions for every call:
+ *   - Every function returns a zero_status; arguments are checked before any
+ *     CUDA work is issued, and a rejected call changes nothing.
+ *   - "device" pointers are CUDA global-memory addresses on the device that
+ *     was current when the handle was created; that device must be current
+ *     for every call on the handle.  "host" pointers are ordinary CPU memory.
+ *   - The library never allocates, frees or retains caller buffers.  Device
+ *     buffers must stay valid until the stream has passed the work that uses
+ *     them.  The handle owns a small device workspace (a few tens of KB).
+ *   - `stream` is a cudaStream_t (NULL is the legacy default stream).  Work is
+ *     enqueued asynchronously unless the function says it synchronizes.
+ *   - Calls on one handle must be ordered (one stream, or externally
+ *     synchronized): they share the handle's workspace.
+ *   - Pointers that are not 16-byte aligned are accepted; they select a
+ *     slower element-wise path instead of 16-byte vector accesses.
+ */
+#ifndef ZERO_OPT_H
+#define ZERO_OPT_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum zero_status {
+  ZERO_OK = 0,
+  ZERO_EINVAL = 1,   /* invalid argument (null pointer, bad value, bad dtype) */
+  ZERO_ERANGE = 2,   /* index or size out of range (rank >= world, ...) */
+  ZERO_ENOMEM = 3,   /* host or device allocation failed in zero_opt_create */
+  ZERO_ECUDA = 4,    /* a CUDA call failed, or no CUDA device is present */
+  ZERO_ENOTSUP = 5   /* option not supported by this build */
+} zero_status;
+
+typedef enum zero_dtype {
+  ZERO_FP16 = 0,     /* IEEE binary16 */
+  ZERO_BF16 = 1      /* bfloat16 */
+} zero_dtype;
+
+typedef struct zero_opt_handle* zero_opt_t;
+
+/*
+ * Optimizer and loss-scale configuration: the fields of a ds_config.json
+ * ("DeepSpeed tutorial" §3.2) that the step needs.  Real numbers are given as
+ * doubles; the per-step scalars derived from them are computed in double and
+ * rounded once to float.
+ */
+typedef struct zero_opt_config {
+  int64_t numel;            /* Ψ: real parameters of the flat buffer (>= 0) */
+  int32_t world;            /* N: data-parallel degree (>= 1)               */
+  int32_t grad_dtype;       /* zero_dtype of the gradient buffers           */
+  int32_t param_dtype;      /* zero_dtype of the 16-bit parameter copy      */
+  int32_t bias_correction;  /* 1: Adam bias correction; 0: none             */
+  double lr;                /* learning rate (>= 0)                         */
+  double beta1, beta2;      /* in [0, 1)                                    */
+  double eps;               /* > 0, added outside the square root           */
+  double weight_decay;      /* >= 0, decoupled (AdamW): p *= 1 - lr*wd      */
+  double max_grad_norm;     /* > 0 clips the global L2 norm; <= 0 disables  */
+  int32_t dynamic_scale;    /* 1: dynamic loss scale; 0: fixed init_scale   */
+  int32_t hysteresis;       /* must be 1 (halve on every overflow)          */
+  double init_scale;        /* > 0, e.g. 2^initial_scale_power              */
+  double min_scale;         /* > 0, "min_loss_scale"                        */
+  double scale_factor;      /* >= 1, 2 halves / doubles                     */
+  int64_t scale_window;     /* >= 1, "loss_scale_window"                    */
+} zero_opt_config;
+
+/*
+ * Buffers of one flat shard step.  Layout: the flat parameter buffer holds Ψ
+ * real elements padded with zeros to P = N * S elements, S = ceil(Ψ / N); rank
+ * r owns [r*S, r*S + S), of which [r*S, real_end) are real ("ZeRO三阶段";
+ * "DeepSpeed tutorial" §2.4).  Only real elements are read or written.
+ */
+typedef struct zero_opt_buffers {
+  float* master;            /* device, fp32 master weights of the shard (S)  */
+  float* m;                 /* device, fp32 first moment of the shard (S)    */
+  float* v;                 /* device, fp32 second moment of the shard (S)   */
+  void* param16;            /* device, 16-bit parameters (param_dtype); the
+                               full padded buffer (P) unless
+                               param16_shard_local, then the shard (S)       */
+  const void* const* grads; /* host array of n_ranks*n_micro device pointers,
+                               rank-major (index r*n_micro + k); each is the
+                               full padded gradient buffer (P) of simulated
+                               rank r and micro-step k, unless
+                               grads_shard_local, then the shard (S)         */
+  int32_t n_ranks;          /* R >= 1: simulated data-parallel ranks         */
+  int32_t n_micro;          /* K >= 1: gradient-accumulation micro-steps     */
+  int32_t grads_shard_local;
+  int32_t param16_shard_local;
+  double divisor;           /* D: the reduced sum is divided by D*scale;
+                               <= 0 selects R*K (the average)                */
+  float* stash;             /* optional device fp32 scratch of S elements: when
+                               R*K > 4 the reduced sum is kept here between the
+                               two passes instead of re-reading R*K buffers;
+                               NULL always re-reads                          */
+} zero_opt_buffers;
+
+/* One tensor of a per-tensor (non-flat) list, all its buffers separate. */
+typedef struct zero_opt_tensor {
+  int64_t numel;            /* elements of this tensor (>= 0)                */
+  float* master;            /* device fp32, numel                            */
+  float* m;                 /* device fp32, numel                            */
+  float* v;                 /* device fp32, numel                            */
+  void* param16;            /* device 16-bit, numel                          */
+  const void* const* grads; /* host array of n_ranks*n_micro device pointers
+                               to this tensor's gradients, rank-major        */
+} zero_opt_tensor;
+
+typedef struct zero_opt_tensor_list {
+  const zero_opt_tensor* tensors;  /* host array of n_tensors entries        */
+  int32_t n_tensors;               /* >= 0                                   */
+  int32_t n_ranks, n_micro;        /* R, K as in zero_opt_buffers            */
+  double divisor;                  /* as in zero_opt_buffers                 */
+  float* stash;                    /* optional device fp32 scratch of the
+                                      summed numel of all tensors, or NULL   */
+} zero_opt_tensor_list;
+
+/* Gradient statistics of one shard, or their fold over all ranks. */
+typedef struct zero_opt_stats {
+  double sumsq;             /* sum of squares of the fp32 reduced (still
+                               scaled) gradient sums                         */
+  int32_t nonfinite;        /* 1 if any reduced gradient is inf or NaN       */
+  int32_t reserved;
+} zero_opt_stats;
+
+/* What the last step of a rank decided (zero_opt_last_step). */
+typedef struct zero_opt_step_info {
+  double sumsq;             /* global sum of squares used                    */
+  double norm;              /* L2 norm of the unscaled gradient (NaN on skip) */
+  float coef;               /* factor applied to each reduced sum            */
+  float scale_used;         /* loss scale the gradients carried              */
+  int32_t skipped;          /* 1 if the step was skipped (overflow)          */
+  int32_t nonfinite;
+  int64_t t;                /* Adam step counter after the step              */
+} zero_opt_step_info;
+
+/* Loss-scaler state of one rank. */
+typedef struct zero_opt_scaler_state {
+  float scale;              /* current loss scale                            */
+  int32_t last_skipped;     /* 1 if the last step was skipped                */
+  int64_t clean_steps;      /* consecutive applied steps since last change   */
+  int64_t t;                /* Adam step counter (applied updates)           */
+  int64_t skipped_total;    /* skipped steps so far                          */
+} zero_opt_scaler_state;
+
+/* Fill *cfg with the ds_config.json values of "DeepSpeed tutorial" §3.2:
+ * AdamW lr 2e-5, betas (0.9, 0.999), eps 1e-8, weight_decay 0.01; dynamic
+ * fp16 loss scale 2^16 (initial_scale_power 16), window 1000, min 1, factor
+ * 2; bias correction on, no clipping; numel 0, world 1, fp16.  Hysteresis is
+ * 1 (the page's value 2 is not supported).  Errors: EINVAL if cfg is NULL. */
+zero_status zero_opt_config_default(zero_opt_config* cfg);
+
+/* Create an optimizer handle for one data-parallel group of `world` ranks.
+ * Each rank r has its own loss-scaler replica (scale = init_scale, counters
+ * 0).  Allocates the handle's device workspace on the current device when a
+ * CUDA device is present; without one the handle serves only the host-side
+ * calls and every launching call returns ZERO_ECUDA.
+ * Errors: EINVAL (NULL pointers, numel < 0, world < 1, a dtype not in
+ * zero_dtype, lr < 0, beta outside [0,1), eps <= 0, weight_decay < 0,
+ * init_scale/min_scale <= 0, scale_factor < 1, scale_window < 1);
+ * ENOTSUP (hysteresis != 1); ENOMEM; ECUDA.  *out is NULL on failure. */
+zero_status zero_opt_create(const zero_opt_config* cfg, zero_opt_t* out);
+
+/* Destroy a handle (synchronizes the device first). NULL is accepted. */
+zero_status zero_opt_destroy(zero_opt_t h);
+
+/* Shard bounds of `rank` ("ZeRO三阶段": N equal parts; padding to P = N*S).
+ * Host only.  Outputs (host, each may be NULL): begin = rank*S, real_end =
+ * min(begin + S, Ψ) (>= begin), shard_len = S, padded_numel = P.
+ * Errors: EINVAL (h NULL), ERANGE (rank outside [0, world)). */
+zero_status zero_opt_shard_bounds(zero_opt_t h, int32_t rank, int64_t* begin,
+                                  int64_t* real_end, int64_t* shard_len,
+                                  int64_t* padded_numel);
+
+/* Per-GPU model-state bytes of ZeRO stage 0..3 for Ψ = numel over N = world
+ * ranks, on the padded shard S = ceil(Ψ/N): stage 0 (DDP) 16Ψ, stage 1
+ * 4Ψ + 12S, stage 2 2Ψ + 14S, stage 3 16S ("LLM-train tutorials ch01" §1.2;
+ * "DeepSpeed tutorial" §2.1).  Equal to the pages' forms when N divides Ψ.
+ * Host only. Errors: EINVAL (bytes NULL, numel < 0, world < 1), ERANGE
+ * (stage outside 0..3). */
+zero_status zero_opt_memory_bytes(int64_t numel, int32_t world, int32_t stage,
+                                  int64_t* bytes);
+
+/* Statistics of `rank`'s shard only (steps a1..a3): the fp32 reduction of
+ * the R*K gradient buffers, its overflow flag and its sum of squares.  This is
+ * the local half of the scalar all-reduce; fold all ranks' results in rank
+ * order (sum sumsq, OR nonfinite) and pass the fold to zero_opt_step.  Also
+ * fills bufs->stash when it is used.  Synchronizes `stream`; *out is host.
+ * Errors: as zero_opt_step. */
+zero_status zero_opt_grad_stats(zero_opt_t h, int32_t rank,
+                                const zero_opt_buffers* bufs, void* stream,
+                                zero_opt_stats* out);
+
+/* The scalar all-reduce of the statistics, done on the host: *out = the fold
+ * of per_rank[0..n) in rank order (binary64 sum of sumsq starting from 0,
+ * OR of nonfinite).  Every rank that folds the same array gets bit-identical
+ * totals, as after an all-reduce ("DeepSpeed framework interview answer",
+ * "ZeRO 三阶段": gradients are reduce-scattered before the local update).
+ * Host only.  Errors: EINVAL (out NULL, n < 0, per_rank NULL with n > 0). */
+zero_status zero_opt_fold_stats(const zero_opt_stats* per_rank, int32_t n,
+                                zero_opt_stats* out);
+
+/* One optimizer step of `rank`'s shard (steps a1..a7), asynchronous on
+ * `stream`.  `global` (host, may be NULL) is the fold of all ranks'
+ * zero_opt_grad_stats for these same gradients; NULL means this shard is the
+ * whole world and its own statistics decide.  On overflow the step is skipped
+ * (master, m, v, param16 and t untouched) and the scale is divided by
+ * scale_factor, not below min_scale; otherwise AdamW is applied and after
+ * scale_window consecutive applied steps the scale is multiplied by
+ * scale_factor ("DeepSpeed tutorial" §2.2, §3.2).
+ * Errors: EINVAL (h/bufs/grads NULL, a NULL state or gradient pointer for a
+ * non-empty shard, R or K < 1, R*K > 1024), ERANGE (rank outside [0, world)),
+ * ECUDA (no device, wrong current device, or a launch failure). */
+zero_status zero_opt_step(zero_opt_t h, int32_t rank, const zero_opt_buffers* bufs,
+                          void* stream, const zero_opt_stats* global);
+
+/* Statistics of a per-tensor list (multi-tensor apply): as
+ * zero_opt_grad_stats, over the concatenation of the tensors in list order.
+ * `rank` selects the loss-scaler replica. Synchronizes `stream`. */
+zero_status zero_opt_grad_stats_tensors(zero_opt_t h, int32_t rank,
+                                        const zero_opt_tensor_list* list,
+                                        void* stream, zero_opt_stats* out);
+
+/* One optimizer step over a per-tensor list: the same math as zero_opt_step,
+ * with the L2 norm and the overflow flag taken over all tensors of the list
+ * (plus the other ranks' through `global`).  Each tensor keeps its own
+ * master/m/v/param16/gradient buffers.  Asynchronous on `stream`.
+ * Errors: as zero_opt_step; EINVAL for n_tensors < 0 or a NULL tensors array
+ * with n_tensors > 0. */
+zero_status zero_opt_step_tensors(zero_opt_t h, int32_t rank,
+                                  const zero_opt_tensor_list* list, void* stream,
+                                  const zero_opt_stats* global);
+
+/* Read `rank`'s loss-scaler state into *out (host).  Synchronizes `stream`.
+ * Errors: EINVAL (NULL), ERANGE (rank), ECUDA. */
+zero_status zero_opt_loss_scale(zero_opt_t h, int32_t rank, void* stream,
+                                zero_opt_scaler_state* out);
+
+/* Overwrite `rank`'s loss-scaler state (resume from a checkpoint), ordered on
+ * `stream`.  Errors: EINVAL (NULL, scale <= 0, negative counters), ERANGE,
+ * ECUDA. */
+zero_status zero_opt_set_loss_scale(zero_opt_t h, int32_t rank, void* stream,
+                                    const zero_opt_scaler_state* in);
+
+/* Set the learning rate for subsequent steps (a scheduler such as WarmupLR,
+ * "DeepSpeed tutorial" §3.2, changes it per step). Host only.
+ * Errors: EINVAL (h NULL, lr < 0). */
+zero_status zero_opt_set_lr(zero_opt_t h, double lr);
+
+/* What the last step (on any rank) of this handle decided.  Synchronizes
+ * `stream`. Errors: EINVAL, ECUDA. */
+zero_status zero_opt_last_step(zero_opt_t h, void* stream, zero_opt_step_info* out);
+
+/* Timing hook: subsequent steps (and statistics calls) of this handle record
+ * the caller's CUDA events (cudaEvent_t, created by the caller; each may be
+ * NULL) on the step's stream: ev_start before pass 1, ev_mid between pass 1
+ * and pass 2, ev_end after pass 2 (after pass 1 when there is no pass 2).
+ * Passing three NULLs turns the hook off.  The events measure each pass on
+ * the stream it runs on.  Host only; records nothing by itself.
+ * Errors: EINVAL (h NULL). */
+zero_status zero_opt_set_events(zero_opt_t h, void* ev_start, void* ev_mid, void* ev_end);
+
+/* Kernels launched by this handle since creation (for launch accounting). */
+zero_status zero_opt_launch_count(zero_opt_t h, int64_t* launches);
+
+/* Static string describing a status code; never NULL. */
+const char* zero_opt_status_string(zero_status s);
+
+/* Message of the last error on this thread (empty if none); never NULL. */
+const char* zero_opt_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,324 @@
+"""GPU parity of the CUDA path (through the C ABI) against the oracle.
+
+Each test runs seeded inputs shaped like one workload at a size the oracle
+finishes in seconds, spanning many 2048-element tiles and a ragged tail, and
+compares element by element: flags, skip decisions, the loss-scale sequence
+and counters bit-exactly; fp32 master/m/v within 1e-6 relative (abs floor
+1e-9); 16-bit parameters within 1 ulp; the gradient norm within 1e-5 relative.
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+import synth
+from harness import (FlatCase, assert_flat_parity, exact_fraction, llama_like_shapes,
+                     run_flat, run_list, ulp16_diff)
+
+pytestmark = pytest.mark.gpu
+
+INF16, NINF16, NAN16 = 0x7C00, 0xFC00, 0x7E00
+INF_BF16 = 0x7F80
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+# ---------------------------------------------------------------- generator
+
+@pytest.mark.parametrize("kind", [synth.F32, synth.F16, synth.BF16])
+def test_synth_gpu_matches_numpy(kind):
+    import torch
+    n, off = 100_003, 777
+    t = synth.normal_torch(7, 3, n, 0.37, kind, device="cuda", offset=off)
+    ref = synth.normal_np(7, 3, off, n, 0.37, kind)
+    got = t.cpu()
+    if kind == synth.F32:
+        assert (got.numpy().view(np.uint32) == ref.view(np.uint32)).all()
+    else:
+        assert (got.view(torch.int16).numpy().view(np.uint16) == ref).all()
+
+
+# ---------------------------------------------------------------- the five workloads
+
+def _tiny_inject():
+    # +inf in one seeded rank's buffer at one seeded real index, on step 4
+    r, j = synth.seeded_indices(0x5EED0001, 99, 1, 0, 4)[0], \
+        synth.seeded_indices(0x5EED0001, 98, 1, 0, 1_000_003)[0]
+    return {4: [(r, j, INF16)]}
+
+
+def test_tiny_n4_ten_steps_with_overflow():
+    """1,000,003 fp16 parameters over 4 simulated ranks (padded to 1,000,004),
+    loss scale 2048, Adam lr 1e-3, +inf on step 4: skip and halve."""
+    case = FlatCase(numel=1_000_003, world=4, ranks=4, gdtype=O.FP16, lr=1e-3,
+                    dynamic=True, init_scale=2048.0, window=1000, sigma=1e-3,
+                    steps=10, inject=_tiny_inject())
+    res = run_flat(case)
+    skips = [h["gpu"][0] for h in res["history"]]
+    scales = [h["gpu"][1] for h in res["history"]]
+    assert skips == [0, 0, 0, 1, 0, 0, 0, 0, 0, 0]
+    assert scales == [2048.0] * 4 + [1024.0] * 6
+    assert res["history"][-1]["gpu"][2] == 9
+    # no clipping: the coefficient does not depend on the norm, so the whole
+    # state must agree bit for bit
+    assert_flat_parity(res, exact=True)
+
+
+def test_tiny_union_of_shards_equals_unsharded():
+    """Four shard steps with folded statistics give bit-identical master/m/v/
+    param16 to one unsharded step over the same four full buffers."""
+    base = dict(numel=1_000_003, ranks=4, gdtype=O.FP16, lr=1e-3, dynamic=True,
+                init_scale=2048.0, sigma=1e-3, steps=3)
+    sh = run_flat(FlatCase(world=4, **base))
+    un = run_flat(FlatCase(world=1, **base))
+    for i in range(4):
+        cat = np.concatenate([sh["gpu"][r][i] for r in range(4)])
+        assert (cat.view(np.uint8) == un["gpu"][0][i].view(np.uint8)).all(), i
+
+
+def test_gpt2_like_bf16_clip():
+    """bf16 gradients ~N(0, 1e-2), N=1, no loss scaling, AdamW lr 3e-4 wd 0.01,
+    global-norm clip 1.0 (active every step), 30 steps; 1,000,003 parameters."""
+    case = FlatCase(numel=1_000_003, world=1, gdtype=O.BF16, lr=3e-4, wd=0.01,
+                    max_norm=1.0, sigma=1e-2, steps=30, seed=0x5EED0002)
+    res = run_flat(case, check_every_step=False)
+    assert all(h["gpu"][3] > 1.0 for h in res["history"])   # clipping active
+    assert_flat_parity(res)
+    assert exact_fraction(res) > 0.99
+
+
+def test_llama_like_zero2_rank0_periodic_overflow():
+    """fp16 gradients ~N(0, 1e-4) x dynamic scale from 2^16, window 1000, rank 0
+    of N=8 with shard-local gradients (after reduce-scatter), inf injected every
+    50 steps, AdamW lr 1e-4 wd 0.1, 100 steps."""
+    S = 262_147
+    inj = {}
+    for k, step in enumerate(range(50, 101, 50)):
+        j = synth.seeded_indices(0x5EED0003, 200 + k, 1, 0, S)[0]
+        inj[step] = [(0, j, INF16)]
+    case = FlatCase(numel=8 * S, world=8, shards=(0,), shard_local_grads=True,
+                    gdtype=O.FP16, lr=1e-4, wd=0.1, dynamic=True, init_scale=2.0 ** 16,
+                    window=1000, sigma=1e-4, steps=100, seed=0x5EED0003, inject=inj)
+    res = run_flat(case, check_every_step=False)
+    sk = [h["step"] for h in res["history"] if h["gpu"][0]]
+    assert sk == [50, 100]
+    assert res["scaler"][0][0] == (2.0 ** 14, 0, 98, 2, 1)
+    assert_flat_parity(res)
+
+
+@pytest.mark.parametrize("stash", [True, False])
+def test_fused_reduce_r8_k4_clip(stash):
+    """8 simulated ranks x 4 micro-steps of fp16 shard gradients ~N(0, 1e-3) x
+    1024, summed and divided by N*K = 32, AdamW lr 2e-4 wd 0.01, clip 1.0."""
+    case = FlatCase(numel=300_007, world=1, ranks=8, micro=4, gdtype=O.FP16, lr=2e-4,
+                    wd=0.01, max_norm=1.0, init_scale=1024.0, sigma=1e-3, steps=3,
+                    divisor=32.0, seed=0x5EED0004, stash=stash, shard_local_grads=True)
+    res = run_flat(case)
+    assert_flat_parity(res)
+
+
+def test_per_tensor_list_llama_shapes():
+    """73 tensors with Llama-3-8B shapes (every dimension / 64): embedding plus
+    8 decoder layers; bf16 gradients ~N(0, 1e-3), AdamW lr 1e-4 wd 0.1, clip 1.0."""
+    shapes = llama_like_shapes(layers=8, div=64)
+    assert len(shapes) == 73
+    numels = [int(np.prod(s)) for s in shapes]
+    res = run_list(numels, steps=3)
+    assert_flat_parity(res)
+
+
+# ---------------------------------------------------------------- edge cases
+
+@pytest.mark.parametrize("n", [1, 7, 8, 9, 2047, 2048, 2049, 4099, 8 * 2048 * 4 + 5])
+def test_sizes_around_the_tile(n):
+    case = FlatCase(numel=n, gdtype=O.FP16, lr=1e-3, wd=0.01, max_norm=0.05,
+                    init_scale=4.0, sigma=1e-2, steps=3)
+    assert_flat_parity(run_flat(case))
+
+
+@pytest.mark.parametrize("numel,world", [(3, 4), (1, 4), (5, 8), (0, 2)])
+def test_all_padding_shards(numel, world):
+    """Shards with no real element still take the global decision and advance
+    their scaler; real shards match the oracle."""
+    case = FlatCase(numel=numel, world=world, ranks=2, gdtype=O.FP16, dynamic=True,
+                    init_scale=8.0, max_norm=0.5, steps=3)
+    res = run_flat(case)
+    assert_flat_parity(res)
+    for r, (g, ref) in res["scaler"].items():
+        assert g[2] == 3
+
+
+@pytest.mark.parametrize("misalign", [1, 3])
+def test_misaligned_buffers_take_the_element_path(misalign):
+    case = FlatCase(numel=50_001, world=3, ranks=2, gdtype=O.BF16, lr=1e-3, wd=0.1,
+                    max_norm=0.3, sigma=1e-2, steps=3, misalign=misalign)
+    assert_flat_parity(run_flat(case))
+
+
+def test_vector_and_element_paths_agree_bit_for_bit():
+    base = dict(numel=40_000, world=1, ranks=3, gdtype=O.FP16, lr=1e-3, wd=0.01,
+                init_scale=64.0, sigma=1e-2, steps=3)
+    a = run_flat(FlatCase(misalign=0, **base))
+    b = run_flat(FlatCase(misalign=1, **base))
+    for x, y in zip(a["gpu"][0], b["gpu"][0]):
+        assert (x.view(np.uint8) == y.view(np.uint8)).all()
+
+
+@pytest.mark.parametrize("inject", [
+    [(0, 1234, INF16)], [(1, 1234, NINF16)], [(0, 99_999, NAN16)],
+    [(0, 5, INF16), (1, 5, NINF16)],
+], ids=["+inf", "-inf", "nan", "+inf-inf"])
+def test_overflow_kinds_skip(inject):
+    case = FlatCase(numel=100_000, world=2, ranks=2, gdtype=O.FP16, dynamic=True,
+                    init_scale=512.0, steps=3, inject={2: inject}, max_norm=1.0)
+    res = run_flat(case)
+    assert [h["gpu"][0] for h in res["history"]] == [0, 1, 0]
+    assert_flat_parity(res)
+
+
+def test_largest_fp16_values_do_not_overflow():
+    inj = {1: [(b, j, 0x7BFF) for b in range(2) for j in range(0, 4096, 7)]}
+    case = FlatCase(numel=10_000, ranks=2, gdtype=O.FP16, init_scale=1.0, steps=2,
+                    inject=inj, max_norm=1.0)
+    res = run_flat(case)
+    assert res["history"][0]["gpu"][0] == 0
+    assert_flat_parity(res)
+
+
+@pytest.mark.parametrize("exp_bits", [0x5C00, 0x1F00], ids=["2^57", "2^-65"])
+def test_extreme_bf16_magnitudes_in_the_norm(exp_bits):
+    """Gradients near 2^57 (squares near the binary32 overflow range) and near
+    2^-65 (squares below binary32's normal range) still give the oracle's norm."""
+    inj = {s: [(0, j, exp_bits | (j & 0x7F)) for j in range(0, 3000, 3)] for s in (1, 2)}
+    case = FlatCase(numel=6000, gdtype=O.BF16, steps=2, max_norm=1.0, sigma=1e-30,
+                    inject=inj)
+    res = run_flat(case)
+    assert_flat_parity(res)
+
+
+def test_stash_and_reread_agree_bit_for_bit():
+    base = dict(numel=70_001, world=1, ranks=4, micro=2, gdtype=O.FP16, lr=1e-3,
+                max_norm=0.5, init_scale=32.0, steps=3, shard_local_grads=True)
+    a = run_flat(FlatCase(stash=True, **base))
+    b = run_flat(FlatCase(stash=False, **base))
+    for x, y in zip(a["gpu"][0], b["gpu"][0]):
+        assert (x.view(np.uint8) == y.view(np.uint8)).all()
+
+
+def test_runs_are_deterministic():
+    case = FlatCase(numel=300_000, world=2, ranks=2, gdtype=O.BF16, max_norm=0.1,
+                    sigma=1e-2, steps=3)
+    a = run_flat(case)
+    b = run_flat(case)
+    assert [h["gpu"] for h in a["history"]] == [h["gpu"] for h in b["history"]]
+    for r in a["gpu"]:
+        for x, y in zip(a["gpu"][r], b["gpu"][r]):
+            assert (x.view(np.uint8) == y.view(np.uint8)).all()
+
+
+def test_resume_is_bit_exact():
+    """Ten steps straight equal five steps, a save of (master, m, v, scaler) and
+    a restore into a fresh handle, then five more steps."""
+    import torch
+
+    import zero_sharded_mixed_05_gb300 as z
+    dev = torch.device("cuda:0")
+    n = 50_000
+    cfg = z.make_config(numel=n, world=1, grad_dtype=z.FP16, lr=1e-3, weight_decay=0.01,
+                        max_grad_norm=0.5, dynamic_scale=True, init_scale=256.0,
+                        scale_window=3)
+    p0 = torch.from_numpy(synth.normal_np(5, 0, 0, n, 0.02, synth.F32)).to(dev)
+    grads = [synth.normal_torch(5, 1, n, 0.5, synth.F16, device=dev, offset=s * n)
+             for s in range(10)]
+    grads[6][17] = float("inf")
+
+    def fresh():
+        return [p0.clone(), torch.zeros(n, device=dev), torch.zeros(n, device=dev),
+                torch.zeros(n, dtype=torch.float16, device=dev)]
+
+    def steps(h, st, lo, hi):
+        for s in range(lo, hi):
+            z.zero_opt_step(h, 0, z.make_buffers(*st, [grads[s]]))
+
+    h1 = z.zero_opt_create(cfg)
+    a = fresh()
+    steps(h1, a, 0, 10)
+    h2 = z.zero_opt_create(cfg)
+    b = fresh()
+    steps(h2, b, 0, 5)
+    saved = [x.clone() for x in b]
+    sc = z.zero_opt_loss_scale(h2, 0)
+    z.zero_opt_destroy(h2)
+    h3 = z.zero_opt_create(cfg)
+    z.zero_opt_set_loss_scale(h3, 0, sc)
+    steps(h3, saved, 5, 10)
+    torch.cuda.synchronize()
+    for x, y in zip(a, saved):
+        assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
+    assert z.zero_opt_loss_scale(h1, 0).as_tuple() == z.zero_opt_loss_scale(h3, 0).as_tuple()
+    z.zero_opt_destroy(h1)
+    z.zero_opt_destroy(h3)
+
+
+def test_local_step_equals_stats_fold_step():
+    """For one shard that is the whole world, the asynchronous local step and
+    the statistics -> fold -> step sequence agree bit for bit."""
+    import torch
+
+    import zero_sharded_mixed_05_gb300 as z
+    dev = torch.device("cuda:0")
+    n = 123_457
+    cfg = z.make_config(numel=n, world=1, grad_dtype=z.BF16, lr=1e-3, max_grad_norm=0.2,
+                        dynamic_scale=False, init_scale=1.0)
+    g = synth.normal_torch(3, 1, n, 1e-2, synth.BF16, device=dev)
+    p0 = torch.from_numpy(synth.normal_np(3, 0, 0, n, 0.02, synth.F32)).to(dev)
+    out = []
+    for use_fold in (False, True):
+        h = z.zero_opt_create(cfg)
+        st = [p0.clone(), torch.zeros(n, device=dev), torch.zeros(n, device=dev),
+              torch.zeros(n, dtype=torch.bfloat16, device=dev)]
+        b = z.make_buffers(*st, [g])
+        for _ in range(3):
+            if use_fold:
+                G = z.zero_opt_fold_stats([z.zero_opt_grad_stats(h, 0, b)])
+                z.zero_opt_step(h, 0, b, global_stats=G)
+            else:
+                z.zero_opt_step(h, 0, b)
+        torch.cuda.synchronize()
+        out.append(st)
+        z.zero_opt_destroy(h)
+    for x, y in zip(*out):
+        assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
+
+
+def test_cast_matches_cuda_intrinsics_sample():
+    """The oracle's RNE casts equal CUDA's conversion on a sample of values,
+    through the 16-bit copy the step writes (lr = 0 keeps master = input)."""
+    import torch
+
+    import zero_sharded_mixed_05_gb300 as z
+    dev = torch.device("cuda:0")
+    rng = np.random.default_rng(11)
+    bits = rng.integers(0, 1 << 32, 1 << 16, dtype=np.uint64).astype(np.uint32)
+    x = bits.view(np.float32)
+    x = np.where(np.isfinite(x) & (np.abs(x) < 6e4), x, 1.0).astype(np.float32)
+    n = x.size
+    for dt, code in ((torch.float16, z.FP16), (torch.bfloat16, z.BF16)):
+        cfg = z.make_config(numel=n, world=1, grad_dtype=code, lr=0.0, weight_decay=0.0,
+                            dynamic_scale=False, init_scale=1.0)
+        h = z.zero_opt_create(cfg)
+        st = [torch.from_numpy(x.copy()).to(dev), torch.zeros(n, device=dev),
+              torch.zeros(n, device=dev), torch.zeros(n, dtype=dt, device=dev)]
+        z.zero_opt_step(h, 0, z.make_buffers(*st, [torch.zeros(n, dtype=dt, device=dev)]))
+        torch.cuda.synchronize()
+        got = st[3].cpu().view(torch.int16).numpy().view(np.uint16)
+        ref = O.f32_to_16(x, O.FP16 if code == z.FP16 else O.BF16)
+        assert (got == ref).all()
+        z.zero_opt_destroy(h)

@@ -1,0 +1,492 @@
+// kernels.cuh -- sm_103a kernels of the per-shard mixed-precision ZeRO step.
+//
+// pass1_kernel (steps a1..a4): each CTA walks its tiles of the shard, sums the
+//   R*K 16-bit gradient buffers per element in binary32 (rank-major order,
+//   starting from +0), optionally stores the sums (the stash), and accumulates
+//   the overflow flag and the sum of squares.  CTAs publish one partial each;
+//   the CTA that finishes last (atomic ticket, no waiting) folds the partials
+//   in CTA order in binary64, takes the per-step decisions (skip, clip
+//   coefficient, Adam scalars) and advances the rank's loss-scaler state.
+// pass2_kernel (steps a5..a7): reads the decision; on a skip every CTA returns
+//   at once; otherwise it applies unscale x clip, AdamW on the fp32 master
+//   copy and m, v, and writes the 16-bit parameter copy.
+//
+// Both passes are HBM-bandwidth bound streaming kernels.  Tiles are 2048
+// elements (256 threads x 8); a thread moves each of its streams with one
+// 16-byte access per tile when every pointer of the run is 16-byte aligned
+// (vector path) and element by element otherwise.  Pass 2 visits its tiles in
+// the reverse of pass 1's order so that the gradients pass 1 touched last are
+// still in L2 when pass 2 starts.
+//
+// Rounding: every binary32 operation of the update is an explicit IEEE
+// round-to-nearest intrinsic (__fmul_rn, __fadd_rn, __fsqrt_rn, __fdiv_rn), so
+// no multiply-add is ever contracted and results do not depend on the
+// compiler's fusion choices; 16-bit stores use __float2half_rn /
+// __float2bfloat16_rn.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "zero_opt_internal.h"
+
+namespace zo {
+
+// ------------------------------------------------------------- 16-bit formats
+template <typename T>
+struct Fmt;
+
+template <>
+struct Fmt<__half> {
+  static __device__ __forceinline__ float dec(unsigned short b) {
+    return __half2float(__ushort_as_half(b));
+  }
+  static __device__ __forceinline__ unsigned short enc(float f) {
+    return __half_as_ushort(__float2half_rn(f));
+  }
+  static __device__ __forceinline__ void dec8(const uint4& u, float (&f)[kVec]) {
+    const __half2* h = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 t = __half22float2(h[i]);
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  }
+  static __device__ __forceinline__ uint4 enc8(const float (&f)[kVec]) {
+    uint4 u;
+    __half2* h = reinterpret_cast<__half2*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+    return u;
+  }
+};
+
+template <>
+struct Fmt<__nv_bfloat16> {
+  static __device__ __forceinline__ float dec(unsigned short b) {
+    return __bfloat162float(__ushort_as_bfloat16(b));
+  }
+  static __device__ __forceinline__ unsigned short enc(float f) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+  }
+  static __device__ __forceinline__ void dec8(const uint4& u, float (&f)[kVec]) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 t = __bfloat1622float2(h[i]);
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  }
+  static __device__ __forceinline__ uint4 enc8(const float (&f)[kVec]) {
+    uint4 u;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    return u;
+  }
+};
+
+// ------------------------------------------------------------- run lookup
+// Tiles of all runs form one index space; a CTA-uniform cursor finds the run
+// of a tile by binary search over the runs' first tiles and keeps it while
+// consecutive tiles stay inside it.
+struct RunCursor {
+  int64_t begin = 0, end = 0;
+  Seg s;
+  __device__ __forceinline__ void seek(const Seg* __restrict__ segs, int nseg,
+                                       int64_t tile) {
+    if (tile >= begin && tile < end) return;
+    int lo = 0, hi = nseg - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (segs[mid].tile0 <= tile) lo = mid;
+      else hi = mid - 1;
+    }
+    s = segs[lo];
+    begin = s.tile0;
+    end = s.tile0 + s.ntiles;
+  }
+};
+
+__device__ __forceinline__ const unsigned short* grad_ptr(const void* const* gptrs,
+                                                          const Seg& s, int b) {
+  const unsigned long long raw =
+      __ldg(reinterpret_cast<const unsigned long long*>(gptrs) + s.gbase + b);
+  return reinterpret_cast<const unsigned short*>(raw);
+}
+
+// ------------------------------------------------------------- sum of squares
+// Per tile the eight squares are accumulated in binary32 with fused
+// multiply-add; the tile partials are summed per thread with Kahan
+// compensation, and hi - c is taken in binary64 at the end, so the thread's
+// total is accurate to about one binary32 rounding per tile partial.  Tiles
+// holding a value of magnitude >= 2^50 (squares near the binary32 overflow
+// range, or inf/NaN) or whose squares all lie below 2^-80 (near underflow) are
+// summed in binary64 instead.  amax (largest |s| bit pattern) gives the
+// overflow flag: inf and NaN patterns are >= 0x7f800000.
+struct SqAcc {
+  float hi = 0.0f, c = 0.0f;
+  double slow = 0.0;
+  uint32_t amax = 0u;
+
+  __device__ __forceinline__ void add(const float (&s)[kVec]) {
+    uint32_t tmax = 0u;
+    float q = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) {
+      tmax = max(tmax, __float_as_uint(s[i]) & 0x7fffffffu);
+      q = __fmaf_rn(s[i], s[i], q);
+    }
+    amax = max(amax, tmax);
+    if (tmax >= 0x58800000u || (q < 0x1p-80f && tmax != 0u)) {
+      double d = 0.0;
+#pragma unroll
+      for (int i = 0; i < kVec; ++i) d = __dadd_rn(d, __dmul_rn((double)s[i], (double)s[i]));
+      slow = __dadd_rn(slow, d);
+    } else {
+      const float y = __fsub_rn(q, c);
+      const float t = __fadd_rn(hi, y);
+      c = __fsub_rn(__fsub_rn(t, hi), y);
+      hi = t;
+    }
+  }
+  __device__ __forceinline__ double total() const {
+    return __dadd_rn(__dsub_rn((double)hi, (double)c), slow);
+  }
+};
+
+// Fixed-shape CTA sum in binary64: the result (valid in thread 0) depends only
+// on the inputs, never on timing.
+__device__ __forceinline__ double block_sum(double x, double* red) {
+  __syncthreads();
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x = __dadd_rn(x, __shfl_down_sync(0xffffffffu, x, off));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = x;
+  __syncthreads();
+  double t = 0.0;
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) t = __dadd_rn(t, red[w]);
+  }
+  return t;
+}
+
+// ------------------------------------------------------------- decisions (a4)
+// Run by one thread of the last CTA.  Scalars are computed in binary64 and
+// rounded once to binary32.  Overflow: skip, scale /= factor (not below
+// min_scale), clean count restarts.  Otherwise: norm of the unscaled gradient,
+// clip coefficient min(1, max_norm / (norm + 1e-6)), Adam step t += 1 with its
+// bias corrections, and the scale grows by the factor after `window`
+// consecutive applied steps.
+__device__ void decide(const Pass1Args& a, double own_sumsq, int own_flag) {
+  Workspace* ws = a.ws;
+  ws->ticket = 0u;
+  if (a.mode == kStatsOnly) {
+    ws->own_sumsq = own_sumsq;
+    ws->own_nonfinite = own_flag;
+    return;
+  }
+  const double sumsq = a.mode == kStepGlobal ? a.g_sumsq : own_sumsq;
+  const int nonfinite = a.mode == kStepGlobal ? a.g_nonfinite : own_flag;
+  RankState st = a.ranks[a.rank];
+  Decision d;
+  d.sumsq = sumsq;
+  d.nonfinite = nonfinite;
+  d.scale_used = st.scale;
+  d.coef = 0.0f;
+  d.step_size = d.isb2 = d.decay = d.b1 = d.omb1 = d.b2 = d.omb2 = d.eps = 0.0f;
+  const float scale = st.scale;
+  const double inv = 1.0 / ((double)scale * a.hp.divisor);
+  if (nonfinite) {
+    d.skip = 1;
+    d.norm = __longlong_as_double(0x7ff8000000000000ll);
+    if (a.hp.dynamic) {
+      double lowered = (double)scale / a.hp.factor;
+      if (lowered < a.hp.min_scale) lowered = a.hp.min_scale;
+      st.scale = (float)lowered;
+    }
+    st.clean = 0;
+    st.skipped_total += 1;
+    st.last_skipped = 1;
+  } else {
+    const double norm = sqrt(sumsq) * inv;
+    double clip = 1.0;
+    if (a.hp.max_norm > 0.0) {
+      clip = a.hp.max_norm / (norm + 1e-6);
+      if (clip > 1.0) clip = 1.0;
+    }
+    d.skip = 0;
+    d.norm = norm;
+    d.coef = (float)(inv * clip);
+    st.t += 1;
+    double bc1 = 1.0, bc2 = 1.0;
+    if (a.hp.bias_correction) {
+      bc1 = 1.0 - pow(a.hp.beta1, (double)st.t);
+      bc2 = 1.0 - pow(a.hp.beta2, (double)st.t);
+    }
+    d.step_size = (float)(a.hp.lr / bc1);
+    d.isb2 = (float)(1.0 / sqrt(bc2));
+    d.decay = (float)(1.0 - a.hp.lr * a.hp.wd);
+    d.b1 = (float)a.hp.beta1;
+    d.omb1 = (float)(1.0 - a.hp.beta1);
+    d.b2 = (float)a.hp.beta2;
+    d.omb2 = (float)(1.0 - a.hp.beta2);
+    d.eps = (float)a.hp.eps;
+    st.last_skipped = 0;
+    st.clean += 1;
+    if (a.hp.dynamic && st.clean == a.hp.window) {
+      st.scale = (float)((double)scale * a.hp.factor);
+      st.clean = 0;
+    }
+  }
+  d.t = st.t;
+  a.ranks[a.rank] = st;
+  ws->dec = d;
+}
+
+// ------------------------------------------------------------- pass 1
+// NB == 1: exactly one gradient buffer; four tiles are loaded before any is
+// reduced so that each thread keeps four 16-byte loads in flight.
+// NB == 0: any number of buffers, loaded in batches of eight per tile.
+template <typename GT, bool STASH, int NB>
+__global__ void __launch_bounds__(kThreads, 4) pass1_kernel(const Pass1Args a) {
+  __shared__ double red[kThreads / 32];
+  __shared__ int s_last;
+  constexpr int U = (NB == 1) ? 4 : 1;
+  const int tid = threadIdx.x;
+  const int64_t G = gridDim.x;
+  SqAcc acc;
+  RunCursor cur;
+
+  for (int64_t t0 = blockIdx.x; t0 < a.ntiles; t0 += U * G) {
+    uint4 raw[U];
+    bool fast[U];
+    if (NB == 1) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t tile = t0 + u * G;
+        fast[u] = false;
+        if (tile < a.ntiles) {
+          cur.seek(a.segs, a.nseg, tile);
+          const int64_t e0 = (tile - cur.s.tile0) * kTile + tid * kVec;
+          if (cur.s.vec && e0 + kVec <= cur.s.n) {
+            raw[u] = __ldcg(reinterpret_cast<const uint4*>(grad_ptr(a.gptrs, cur.s, 0) + e0));
+            fast[u] = true;
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t tile = t0 + u * G;
+      if (tile >= a.ntiles) continue;
+      cur.seek(a.segs, a.nseg, tile);
+      const Seg& s = cur.s;
+      const int64_t base = (tile - s.tile0) * kTile;
+      const int64_t e0 = base + tid * kVec;
+      const bool vec = s.vec && e0 + kVec <= s.n;
+      float x[kVec];
+      if (NB == 1 && fast[u]) {
+        Fmt<GT>::dec8(raw[u], x);
+#pragma unroll
+        for (int i = 0; i < kVec; ++i) x[i] = __fadd_rn(0.0f, x[i]);
+      } else if (NB != 1 && vec) {
+#pragma unroll
+        for (int i = 0; i < kVec; ++i) x[i] = 0.0f;
+        for (int b0 = 0; b0 < a.nbuf; b0 += 8) {
+          uint4 r[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (b0 + j < a.nbuf)
+              r[j] = __ldcg(reinterpret_cast<const uint4*>(grad_ptr(a.gptrs, s, b0 + j) + e0));
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (b0 + j < a.nbuf) {
+              float y[kVec];
+              Fmt<GT>::dec8(r[j], y);
+#pragma unroll
+              for (int i = 0; i < kVec; ++i) x[i] = __fadd_rn(x[i], y[i]);
+            }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < kVec; ++i) {
+          const int64_t e = s.vec ? e0 + i : base + (int64_t)i * kThreads + tid;
+          float sum = 0.0f;
+          if (e < s.n) {
+            for (int b = 0; b < a.nbuf; ++b)
+              sum = __fadd_rn(sum, Fmt<GT>::dec(__ldcg(grad_ptr(a.gptrs, s, b) + e)));
+          }
+          x[i] = sum;
+        }
+      }
+      if (STASH) {
+        float* dst = a.stash + s.stash_off;
+        if (vec) {
+          reinterpret_cast<float4*>(dst + e0)[0] = make_float4(x[0], x[1], x[2], x[3]);
+          reinterpret_cast<float4*>(dst + e0)[1] = make_float4(x[4], x[5], x[6], x[7]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < kVec; ++i) {
+            const int64_t e = s.vec ? e0 + i : base + (int64_t)i * kThreads + tid;
+            if (e < s.n) dst[e] = x[i];
+          }
+        }
+      }
+      acc.add(x);
+    }
+  }
+
+  const double mine = acc.total();
+  const int flag = acc.amax >= 0x7f800000u ? 1 : 0;
+  const double blk = block_sum(mine, red);
+  const int any = __syncthreads_or(flag);
+  if (tid == 0) {
+    a.ws->part_sumsq[blockIdx.x] = blk;
+    a.ws->part_flag[blockIdx.x] = any;
+    __threadfence();
+    const unsigned int prev = atomicAdd(&a.ws->ticket, 1u);
+    s_last = (prev == gridDim.x - 1) ? 1 : 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  double part = 0.0;
+  int f = 0;
+  for (int c = tid; c < (int)gridDim.x; c += kThreads) {
+    part = __dadd_rn(part, __ldcg(&a.ws->part_sumsq[c]));
+    f |= __ldcg(&a.ws->part_flag[c]);
+  }
+  const double tot = block_sum(part, red);
+  const int anyf = __syncthreads_or(f);
+  if (tid == 0) decide(a, tot, anyf);
+}
+
+// ------------------------------------------------------------- pass 2
+struct Scalars {
+  float coef, b1, omb1, b2, omb2, isb2, eps, decay, step_size;
+};
+
+// a5..a6 for one element: the exact binary32 operation sequence of the step.
+__device__ __forceinline__ void adam_elem(float sj, float& p, float& m, float& v,
+                                          const Scalars& c) {
+  const float g = __fmul_rn(sj, c.coef);
+  m = __fadd_rn(__fmul_rn(c.b1, m), __fmul_rn(c.omb1, g));
+  v = __fadd_rn(__fmul_rn(c.b2, v), __fmul_rn(c.omb2, __fmul_rn(g, g)));
+  const float den = __fadd_rn(__fmul_rn(__fsqrt_rn(v), c.isb2), c.eps);
+  p = __fmul_rn(p, c.decay);
+  p = __fsub_rn(p, __fmul_rn(c.step_size, __fdiv_rn(m, den)));
+}
+
+__device__ __forceinline__ void f4_to(const float4& a, float* d) {
+  d[0] = a.x; d[1] = a.y; d[2] = a.z; d[3] = a.w;
+}
+
+// SRC == 1: one gradient buffer; SRC == 0: a.nbuf buffers; SRC == -1: stash.
+template <typename GT, typename PT, int SRC>
+__global__ void __launch_bounds__(kThreads, 4) pass2_kernel(const Pass2Args a) {
+  const Decision* dp = a.dec;
+  if (dp->skip) return;
+  Scalars c;
+  c.coef = dp->coef;
+  c.b1 = dp->b1;
+  c.omb1 = dp->omb1;
+  c.b2 = dp->b2;
+  c.omb2 = dp->omb2;
+  c.isb2 = dp->isb2;
+  c.eps = dp->eps;
+  c.decay = dp->decay;
+  c.step_size = dp->step_size;
+  const int tid = threadIdx.x;
+  const int64_t G = gridDim.x;
+  if ((int64_t)blockIdx.x >= a.ntiles) return;
+  const int64_t cnt = (a.ntiles - 1 - blockIdx.x) / G + 1;
+  RunCursor cur;
+  for (int64_t k = cnt - 1; k >= 0; --k) {
+    const int64_t tile = blockIdx.x + k * G;
+    cur.seek(a.segs, a.nseg, tile);
+    const Seg& s = cur.s;
+    const int64_t base = (tile - s.tile0) * kTile;
+    const int64_t e0 = base + tid * kVec;
+    if (s.vec && e0 + kVec <= s.n) {
+      float x[kVec], p[kVec], m[kVec], v[kVec];
+      if (SRC == -1) {
+        const float4* st = reinterpret_cast<const float4*>(a.stash + s.stash_off + e0);
+        f4_to(__ldcs(st), x);
+        f4_to(__ldcs(st + 1), x + 4);
+      } else if (SRC == 1) {
+        Fmt<GT>::dec8(__ldcs(reinterpret_cast<const uint4*>(grad_ptr(a.gptrs, s, 0) + e0)), x);
+#pragma unroll
+        for (int i = 0; i < kVec; ++i) x[i] = __fadd_rn(0.0f, x[i]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kVec; ++i) x[i] = 0.0f;
+        for (int b0 = 0; b0 < a.nbuf; b0 += 8) {
+          uint4 r[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (b0 + j < a.nbuf)
+              r[j] = __ldcs(reinterpret_cast<const uint4*>(grad_ptr(a.gptrs, s, b0 + j) + e0));
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (b0 + j < a.nbuf) {
+              float y[kVec];
+              Fmt<GT>::dec8(r[j], y);
+#pragma unroll
+              for (int i = 0; i < kVec; ++i) x[i] = __fadd_rn(x[i], y[i]);
+            }
+          }
+        }
+      }
+      const float4* pm = reinterpret_cast<const float4*>(s.master + e0);
+      const float4* mm = reinterpret_cast<const float4*>(s.m + e0);
+      const float4* vm = reinterpret_cast<const float4*>(s.v + e0);
+      f4_to(__ldcs(pm), p);
+      f4_to(__ldcs(pm + 1), p + 4);
+      f4_to(__ldcs(mm), m);
+      f4_to(__ldcs(mm + 1), m + 4);
+      f4_to(__ldcs(vm), v);
+      f4_to(__ldcs(vm + 1), v + 4);
+#pragma unroll
+      for (int i = 0; i < kVec; ++i) adam_elem(x[i], p[i], m[i], v[i], c);
+      float4* po = reinterpret_cast<float4*>(s.master + e0);
+      float4* mo = reinterpret_cast<float4*>(s.m + e0);
+      float4* vo = reinterpret_cast<float4*>(s.v + e0);
+      __stcs(po, make_float4(p[0], p[1], p[2], p[3]));
+      __stcs(po + 1, make_float4(p[4], p[5], p[6], p[7]));
+      __stcs(mo, make_float4(m[0], m[1], m[2], m[3]));
+      __stcs(mo + 1, make_float4(m[4], m[5], m[6], m[7]));
+      __stcs(vo, make_float4(v[0], v[1], v[2], v[3]));
+      __stcs(vo + 1, make_float4(v[4], v[5], v[6], v[7]));
+      __stcs(reinterpret_cast<uint4*>(static_cast<unsigned short*>(s.p16) + e0),
+             Fmt<PT>::enc8(p));
+    } else {
+#pragma unroll
+      for (int i = 0; i < kVec; ++i) {
+        const int64_t e = s.vec ? e0 + i : base + (int64_t)i * kThreads + tid;
+        if (e >= s.n) continue;
+        float x;
+        if (SRC == -1) {
+          x = __ldcs(a.stash + s.stash_off + e);
+        } else {
+          x = 0.0f;
+          for (int b = 0; b < a.nbuf; ++b)
+            x = __fadd_rn(x, Fmt<GT>::dec(__ldcs(grad_ptr(a.gptrs, s, b) + e)));
+        }
+        float p = __ldcs(s.master + e), m = __ldcs(s.m + e), v = __ldcs(s.v + e);
+        adam_elem(x, p, m, v, c);
+        __stcs(s.master + e, p);
+        __stcs(s.m + e, m);
+        __stcs(s.v + e, v);
+        static_cast<unsigned short*>(s.p16)[e] = Fmt<PT>::enc(p);
+      }
+    }
+  }
+}
+
+}  // namespace zo

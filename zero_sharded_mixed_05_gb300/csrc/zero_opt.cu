@@ -1,0 +1,752 @@
+// zero_opt.cu -- host side of the C ABI declared in include/zero_opt.h.
+//
+// The host code validates arguments, turns the caller's buffers into a "plan"
+// (a device table of runs: the shard of a flat buffer or the tensors of a
+// per-tensor list, each with its gradient pointers), and launches the two
+// passes of kernels.cuh on the caller's stream.  Plans are cached by content,
+// so a training loop that passes the same buffers every step uploads its table
+// once.  The loss-scaler state of every rank lives in the handle's device
+// workspace and is only advanced by the kernels, so a step never waits for the
+// host.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "kernels.cuh"
+#include "zero_opt.h"
+
+namespace {
+
+thread_local std::string g_err;
+
+zero_status fail(zero_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+zero_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(ZERO_ECUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// One run of elements as the caller described it.
+struct HostRun {
+  float* master;
+  float* m;
+  float* v;
+  void* p16;
+  int64_t n;
+  int64_t stash_off;
+  std::vector<const void*> g;
+};
+
+struct Plan {
+  std::vector<unsigned char> blob;  // [Seg x nseg][const void* x nseg*nbuf]
+  void* dev = nullptr;
+  int nseg = 0;
+  int nbuf = 0;
+  int64_t ntiles = 0;
+  uint64_t stamp = 0;
+};
+
+constexpr size_t kMaxPlans = 64;
+
+}  // namespace
+
+struct zero_opt_handle {
+  zero_opt_config cfg;
+  bool has_device = false;
+  int device = -1;
+  int sms = 0;
+  zo::Workspace* ws = nullptr;
+  zo::RankState* ranks = nullptr;
+  void* pinned = nullptr;  // page-locked staging for small reads
+  int64_t launches = 0;
+  uint64_t clock = 0;
+  cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};  // timing hook
+  std::vector<Plan*> plans;
+  std::vector<std::pair<const void*, int>> occ;  // kernel -> CTAs per SM
+  std::mutex mu;
+};
+
+namespace {
+
+constexpr size_t kPinnedBytes = 256;
+
+zero_status check_config(const zero_opt_config* c) {
+  if (c->numel < 0) return fail(ZERO_EINVAL, "numel must be >= 0");
+  if (c->world < 1) return fail(ZERO_EINVAL, "world must be >= 1");
+  if ((c->grad_dtype != ZERO_FP16 && c->grad_dtype != ZERO_BF16) ||
+      (c->param_dtype != ZERO_FP16 && c->param_dtype != ZERO_BF16))
+    return fail(ZERO_EINVAL, "dtype must be ZERO_FP16 or ZERO_BF16");
+  if (!(c->lr >= 0.0)) return fail(ZERO_EINVAL, "lr must be >= 0");
+  if (!(c->beta1 >= 0.0 && c->beta1 < 1.0) || !(c->beta2 >= 0.0 && c->beta2 < 1.0))
+    return fail(ZERO_EINVAL, "betas must lie in [0, 1)");
+  if (!(c->eps > 0.0)) return fail(ZERO_EINVAL, "eps must be > 0");
+  if (!(c->weight_decay >= 0.0)) return fail(ZERO_EINVAL, "weight_decay must be >= 0");
+  if (std::isnan(c->max_grad_norm)) return fail(ZERO_EINVAL, "max_grad_norm is NaN");
+  if (!(c->init_scale > 0.0) || !(c->min_scale > 0.0))
+    return fail(ZERO_EINVAL, "init_scale and min_scale must be > 0");
+  if (!(c->scale_factor >= 1.0)) return fail(ZERO_EINVAL, "scale_factor must be >= 1");
+  if (c->scale_window < 1) return fail(ZERO_EINVAL, "scale_window must be >= 1");
+  if (c->bias_correction != 0 && c->bias_correction != 1)
+    return fail(ZERO_EINVAL, "bias_correction must be 0 or 1");
+  if (c->dynamic_scale != 0 && c->dynamic_scale != 1)
+    return fail(ZERO_EINVAL, "dynamic_scale must be 0 or 1");
+  if (c->hysteresis != 1) return fail(ZERO_ENOTSUP, "hysteresis must be 1");
+  return ZERO_OK;
+}
+
+void shard_of(const zero_opt_config& c, int rank, int64_t* begin, int64_t* real_end,
+              int64_t* shard, int64_t* padded) {
+  const int64_t S = (c.numel + c.world - 1) / c.world;
+  const int64_t b = (int64_t)rank * S;
+  int64_t e = std::min(b + S, c.numel);
+  if (e < b) e = b;
+  *begin = b;
+  *real_end = e;
+  *shard = S;
+  *padded = S * c.world;
+}
+
+zero_status check_handle_rank(zero_opt_t h, int32_t rank) {
+  if (!h) return fail(ZERO_EINVAL, "handle is NULL");
+  if (rank < 0 || rank >= h->cfg.world)
+    return fail(ZERO_ERANGE, "rank %d outside [0, %d)", rank, h->cfg.world);
+  return ZERO_OK;
+}
+
+zero_status check_device(zero_opt_t h) {
+  if (!h->has_device) return fail(ZERO_ECUDA, "no CUDA device for this handle");
+  int cur = -1;
+  cudaError_t e = cudaGetDevice(&cur);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (cur != h->device)
+    return fail(ZERO_ECUDA, "current device %d is not the handle's device %d", cur, h->device);
+  return ZERO_OK;
+}
+
+int occupancy(zero_opt_t h, const void* fn) {
+  for (auto& kv : h->occ)
+    if (kv.first == fn) return kv.second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, zo::kThreads, 0) != cudaSuccess ||
+      n < 1)
+    n = 1;
+  h->occ.emplace_back(fn, n);
+  return n;
+}
+
+bool run_is_vec(const HostRun& r, const float* stash) {
+  if (!aligned16(r.master) || !aligned16(r.m) || !aligned16(r.v) || !aligned16(r.p16))
+    return false;
+  for (const void* g : r.g)
+    if (!aligned16(g)) return false;
+  if (stash && !aligned16(stash + r.stash_off)) return false;
+  return true;
+}
+
+// Serialize the runs into the device table layout; find the identical table
+// in the cache or upload a new one (ordered on `stream`).
+zero_status get_plan(zero_opt_t h, const std::vector<HostRun>& runs, int nbuf,
+                     const float* stash, cudaStream_t stream, Plan** out) {
+  const int nseg = (int)runs.size();
+  std::vector<zo::Seg> segs(nseg);
+  std::vector<const void*> gp;
+  gp.reserve((size_t)nseg * nbuf);
+  int64_t tile0 = 0;
+  for (int i = 0; i < nseg; ++i) {
+    const HostRun& r = runs[i];
+    zo::Seg& s = segs[i];
+    std::memset(&s, 0, sizeof(s));
+    s.master = r.master;
+    s.m = r.m;
+    s.v = r.v;
+    s.p16 = r.p16;
+    s.n = r.n;
+    s.tile0 = tile0;
+    s.ntiles = (r.n + zo::kTile - 1) / zo::kTile;
+    s.stash_off = r.stash_off;
+    s.gbase = (int32_t)gp.size();
+    s.vec = run_is_vec(r, stash) ? 1 : 0;
+    tile0 += s.ntiles;
+    for (const void* g : r.g) gp.push_back(g);
+  }
+  std::vector<unsigned char> blob(sizeof(zo::Seg) * nseg + sizeof(void*) * gp.size());
+  if (!blob.empty()) {
+    std::memcpy(blob.data(), segs.data(), sizeof(zo::Seg) * nseg);
+    std::memcpy(blob.data() + sizeof(zo::Seg) * nseg, gp.data(), sizeof(void*) * gp.size());
+  }
+  std::lock_guard<std::mutex> lock(h->mu);
+  h->clock += 1;
+  for (Plan* p : h->plans) {
+    if (p->nbuf == nbuf && p->nseg == nseg && p->blob == blob) {
+      p->stamp = h->clock;
+      *out = p;
+      return ZERO_OK;
+    }
+  }
+  if (h->plans.size() >= kMaxPlans) {
+    auto it = std::min_element(h->plans.begin(), h->plans.end(),
+                               [](const Plan* a, const Plan* b) { return a->stamp < b->stamp; });
+    Plan* old = *it;
+    if (old->dev) cudaFree(old->dev);  // waits for any work still reading it
+    delete old;
+    h->plans.erase(it);
+  }
+  Plan* p = new Plan;
+  p->blob = std::move(blob);
+  p->nseg = nseg;
+  p->nbuf = nbuf;
+  p->ntiles = tile0;
+  p->stamp = h->clock;
+  if (!p->blob.empty()) {
+    cudaError_t e = cudaMalloc(&p->dev, p->blob.size());
+    if (e != cudaSuccess) {
+      delete p;
+      return cuda_fail(e, "cudaMalloc(plan)");
+    }
+    // From pageable memory: staged before the call returns, and ordered on
+    // `stream` before the kernels that read the table.
+    e = cudaMemcpyAsync(p->dev, p->blob.data(), p->blob.size(), cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) {
+      cudaFree(p->dev);
+      delete p;
+      return cuda_fail(e, "cudaMemcpyAsync(plan)");
+    }
+  }
+  h->plans.push_back(p);
+  *out = p;
+  return ZERO_OK;
+}
+
+using Pass1Fn = void (*)(zo::Pass1Args);
+using Pass2Fn = void (*)(zo::Pass2Args);
+
+Pass1Fn pick_pass1(int gdt, bool stash, bool one) {
+  if (gdt == ZERO_FP16) {
+    if (stash) return one ? zo::pass1_kernel<__half, true, 1> : zo::pass1_kernel<__half, true, 0>;
+    return one ? zo::pass1_kernel<__half, false, 1> : zo::pass1_kernel<__half, false, 0>;
+  }
+  if (stash)
+    return one ? zo::pass1_kernel<__nv_bfloat16, true, 1>
+               : zo::pass1_kernel<__nv_bfloat16, true, 0>;
+  return one ? zo::pass1_kernel<__nv_bfloat16, false, 1>
+             : zo::pass1_kernel<__nv_bfloat16, false, 0>;
+}
+
+template <typename GT, typename PT>
+Pass2Fn pick_pass2_t(int src) {
+  if (src == -1) return zo::pass2_kernel<GT, PT, -1>;
+  if (src == 1) return zo::pass2_kernel<GT, PT, 1>;
+  return zo::pass2_kernel<GT, PT, 0>;
+}
+
+Pass2Fn pick_pass2(int gdt, int pdt, int src) {
+  if (gdt == ZERO_FP16)
+    return pdt == ZERO_FP16 ? pick_pass2_t<__half, __half>(src)
+                            : pick_pass2_t<__half, __nv_bfloat16>(src);
+  return pdt == ZERO_FP16 ? pick_pass2_t<__nv_bfloat16, __half>(src)
+                          : pick_pass2_t<__nv_bfloat16, __nv_bfloat16>(src);
+}
+
+zo::Hyper hyper_of(const zero_opt_config& c, double divisor) {
+  zo::Hyper hp;
+  hp.lr = c.lr;
+  hp.beta1 = c.beta1;
+  hp.beta2 = c.beta2;
+  hp.eps = c.eps;
+  hp.wd = c.weight_decay;
+  hp.max_norm = c.max_grad_norm;
+  hp.divisor = divisor;
+  hp.min_scale = c.min_scale;
+  hp.factor = c.scale_factor;
+  hp.window = c.scale_window;
+  hp.bias_correction = c.bias_correction;
+  hp.dynamic = c.dynamic_scale;
+  return hp;
+}
+
+zero_status launch_kernel(zero_opt_t h, const void* fn, int grid, void* args,
+                          cudaStream_t stream) {
+  void* params[] = {args};
+  cudaError_t e = cudaLaunchKernel(fn, dim3(grid), dim3(zo::kThreads), params, 0, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernel");
+  h->launches += 1;
+  return ZERO_OK;
+}
+
+// Pass 1 (always: it takes the decision), then pass 2 unless only the
+// statistics are wanted.
+zero_status run(zero_opt_t h, int32_t rank, const std::vector<HostRun>& runs, int nbuf,
+                double divisor, float* stash, void* stream_v, zo::Mode mode,
+                const zero_opt_stats* global) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  float* use_stash = (stash != nullptr && nbuf > 4) ? stash : nullptr;
+  Plan* plan = nullptr;
+  zero_status st = get_plan(h, runs, nbuf, use_stash, stream, &plan);
+  if (st != ZERO_OK) return st;
+
+  const zo::Seg* segs = static_cast<const zo::Seg*>(plan->dev);
+  const void* const* gptrs = reinterpret_cast<const void* const*>(
+      static_cast<const unsigned char*>(plan->dev) + sizeof(zo::Seg) * plan->nseg);
+
+  zo::Pass1Args a1;
+  std::memset(&a1, 0, sizeof(a1));
+  a1.segs = segs;
+  a1.gptrs = gptrs;
+  a1.nseg = plan->nseg;
+  a1.nbuf = nbuf;
+  // With the global statistics given and nothing to stash, pass 1 only
+  // decides: one CTA, no tiles.
+  const bool reduce = !(mode == zo::kStepGlobal && use_stash == nullptr);
+  a1.ntiles = reduce ? plan->ntiles : 0;
+  a1.stash = use_stash;
+  a1.mode = mode;
+  a1.rank = rank;
+  if (global) {
+    a1.g_sumsq = global->sumsq;
+    a1.g_nonfinite = global->nonfinite ? 1 : 0;
+  }
+  a1.hp = hyper_of(h->cfg, divisor);
+  a1.ws = h->ws;
+  a1.ranks = h->ranks;
+
+  const void* f1 = reinterpret_cast<const void*>(
+      pick_pass1(h->cfg.grad_dtype, use_stash != nullptr, nbuf == 1));
+  int64_t g1 = (int64_t)occupancy(h, f1) * h->sms;
+  g1 = std::min<int64_t>(g1, std::max<int64_t>(a1.ntiles, 1));
+  g1 = std::min<int64_t>(g1, zo::kMaxCtas);
+  if (h->ev[0]) cudaEventRecord(h->ev[0], stream);
+  st = launch_kernel(h, f1, (int)g1, &a1, stream);
+  if (h->ev[1]) cudaEventRecord(h->ev[1], stream);
+  if (st != ZERO_OK || mode == zo::kStatsOnly || plan->ntiles == 0) {
+    if (h->ev[2]) cudaEventRecord(h->ev[2], stream);
+    return st;
+  }
+
+  zo::Pass2Args a2;
+  std::memset(&a2, 0, sizeof(a2));
+  a2.segs = segs;
+  a2.gptrs = gptrs;
+  a2.nseg = plan->nseg;
+  a2.nbuf = nbuf;
+  a2.ntiles = plan->ntiles;
+  a2.stash = use_stash;
+  a2.dec = &h->ws->dec;
+  const int src = use_stash ? -1 : (nbuf == 1 ? 1 : 0);
+  const void* f2 = reinterpret_cast<const void*>(
+      pick_pass2(h->cfg.grad_dtype, h->cfg.param_dtype, src));
+  int64_t g2 = (int64_t)occupancy(h, f2) * h->sms;
+  g2 = std::min<int64_t>(g2, plan->ntiles);
+  st = launch_kernel(h, f2, (int)g2, &a2, stream);
+  if (h->ev[2]) cudaEventRecord(h->ev[2], stream);
+  return st;
+}
+
+// ---- turning the caller's descriptions into runs
+
+zero_status check_grads(const void* const* grads, int nbuf, bool need_nonnull) {
+  if (!grads) return fail(ZERO_EINVAL, "grads array is NULL");
+  if (need_nonnull)
+    for (int b = 0; b < nbuf; ++b)
+      if (!grads[b]) return fail(ZERO_EINVAL, "gradient pointer %d is NULL", b);
+  return ZERO_OK;
+}
+
+zero_status check_rk(int32_t R, int32_t K) {
+  if (R < 1 || K < 1) return fail(ZERO_EINVAL, "n_ranks and n_micro must be >= 1");
+  if ((int64_t)R * K > zo::kMaxBufs)
+    return fail(ZERO_EINVAL, "n_ranks * n_micro must be <= %d", zo::kMaxBufs);
+  return ZERO_OK;
+}
+
+zero_status flat_runs(zero_opt_t h, int32_t rank, const zero_opt_buffers* b,
+                      std::vector<HostRun>* runs, int* nbuf, double* divisor) {
+  if (!b) return fail(ZERO_EINVAL, "buffers are NULL");
+  zero_status st = check_rk(b->n_ranks, b->n_micro);
+  if (st != ZERO_OK) return st;
+  const int nb = b->n_ranks * b->n_micro;
+  int64_t begin, end, S, P;
+  shard_of(h->cfg, rank, &begin, &end, &S, &P);
+  const int64_t n = end - begin;
+  st = check_grads(b->grads, nb, n > 0);
+  if (st != ZERO_OK) return st;
+  if (n > 0 && (!b->master || !b->m || !b->v || !b->param16))
+    return fail(ZERO_EINVAL, "master, m, v and param16 must be non-NULL");
+  *nbuf = nb;
+  *divisor = b->divisor > 0.0 ? b->divisor : (double)nb;
+  runs->clear();
+  if (n == 0) return ZERO_OK;
+  HostRun r;
+  r.master = b->master;
+  r.m = b->m;
+  r.v = b->v;
+  r.p16 = static_cast<unsigned char*>(b->param16) + (b->param16_shard_local ? 0 : begin * 2);
+  r.n = n;
+  r.stash_off = 0;
+  const int64_t goff = b->grads_shard_local ? 0 : begin * 2;
+  for (int i = 0; i < nb; ++i)
+    r.g.push_back(static_cast<const unsigned char*>(b->grads[i]) + goff);
+  runs->push_back(std::move(r));
+  return ZERO_OK;
+}
+
+zero_status list_runs(const zero_opt_tensor_list* l, std::vector<HostRun>* runs, int* nbuf,
+                      double* divisor) {
+  if (!l) return fail(ZERO_EINVAL, "tensor list is NULL");
+  if (l->n_tensors < 0) return fail(ZERO_EINVAL, "n_tensors must be >= 0");
+  if (l->n_tensors > 0 && !l->tensors) return fail(ZERO_EINVAL, "tensors array is NULL");
+  zero_status st = check_rk(l->n_ranks, l->n_micro);
+  if (st != ZERO_OK) return st;
+  const int nb = l->n_ranks * l->n_micro;
+  runs->clear();
+  int64_t off = 0;
+  for (int i = 0; i < l->n_tensors; ++i) {
+    const zero_opt_tensor& t = l->tensors[i];
+    if (t.numel < 0) return fail(ZERO_EINVAL, "tensor %d has numel < 0", i);
+    if (t.numel > 0) {
+      if (!t.master || !t.m || !t.v || !t.param16)
+        return fail(ZERO_EINVAL, "tensor %d: master, m, v and param16 must be non-NULL", i);
+      st = check_grads(t.grads, nb, true);
+      if (st != ZERO_OK) return st;
+      HostRun r;
+      r.master = t.master;
+      r.m = t.m;
+      r.v = t.v;
+      r.p16 = t.param16;
+      r.n = t.numel;
+      r.stash_off = off;
+      for (int b = 0; b < nb; ++b) r.g.push_back(t.grads[b]);
+      runs->push_back(std::move(r));
+    }
+    off += t.numel;
+  }
+  *nbuf = nb;
+  *divisor = l->divisor > 0.0 ? l->divisor : (double)nb;
+  return ZERO_OK;
+}
+
+zero_status read_small(zero_opt_t h, const void* dev_src, size_t bytes, void* stream_v,
+                       void* out) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
+  cudaError_t e = cudaMemcpyAsync(h->pinned, dev_src, bytes, cudaMemcpyDeviceToHost, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
+  e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  std::memcpy(out, h->pinned, bytes);
+  return ZERO_OK;
+}
+
+}  // namespace
+
+// ====================================================================== ABI
+
+extern "C" {
+
+zero_status zero_opt_config_default(zero_opt_config* c) {
+  if (!c) return fail(ZERO_EINVAL, "cfg is NULL");
+  std::memset(c, 0, sizeof(*c));
+  c->numel = 0;
+  c->world = 1;
+  c->grad_dtype = ZERO_FP16;
+  c->param_dtype = ZERO_FP16;
+  c->bias_correction = 1;
+  c->lr = 2e-5;
+  c->beta1 = 0.9;
+  c->beta2 = 0.999;
+  c->eps = 1e-8;
+  c->weight_decay = 0.01;
+  c->max_grad_norm = 0.0;
+  c->dynamic_scale = 1;
+  c->hysteresis = 1;
+  c->init_scale = 65536.0;
+  c->min_scale = 1.0;
+  c->scale_factor = 2.0;
+  c->scale_window = 1000;
+  return ZERO_OK;
+}
+
+zero_status zero_opt_create(const zero_opt_config* cfg, zero_opt_t* out) {
+  if (!out) return fail(ZERO_EINVAL, "out is NULL");
+  *out = nullptr;
+  if (!cfg) return fail(ZERO_EINVAL, "cfg is NULL");
+  zero_status st = check_config(cfg);
+  if (st != ZERO_OK) return st;
+  zero_opt_handle* h = new (std::nothrow) zero_opt_handle;
+  if (!h) return fail(ZERO_ENOMEM, "handle allocation failed");
+  h->cfg = *cfg;
+  int count = 0;
+  if (cudaGetDeviceCount(&count) != cudaSuccess || count < 1) {
+    cudaGetLastError();  // clear the sticky "no device" error
+    *out = h;            // host-only handle
+    return ZERO_OK;
+  }
+  cudaError_t e = cudaGetDevice(&h->device);
+  if (e == cudaSuccess)
+    e = cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, h->device);
+  const size_t ws_bytes = sizeof(zo::Workspace) + sizeof(zo::RankState) * (size_t)cfg->world;
+  void* ws = nullptr;
+  if (e == cudaSuccess) e = cudaMalloc(&ws, ws_bytes);
+  if (e != cudaSuccess) {
+    delete h;
+    return e == cudaErrorMemoryAllocation ? fail(ZERO_ENOMEM, "workspace allocation failed")
+                                          : cuda_fail(e, "zero_opt_create");
+  }
+  h->ws = static_cast<zo::Workspace*>(ws);
+  h->ranks = reinterpret_cast<zo::RankState*>(static_cast<unsigned char*>(ws) +
+                                              sizeof(zo::Workspace));
+  std::vector<unsigned char> init(ws_bytes, 0);
+  zo::RankState* r0 =
+      reinterpret_cast<zo::RankState*>(init.data() + sizeof(zo::Workspace));
+  for (int r = 0; r < cfg->world; ++r) {
+    r0[r].scale = (float)cfg->init_scale;
+    r0[r].last_skipped = 0;
+    r0[r].clean = 0;
+    r0[r].t = 0;
+    r0[r].skipped_total = 0;
+  }
+  e = cudaMemcpy(ws, init.data(), ws_bytes, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMallocHost(&h->pinned, kPinnedBytes);
+  if (e != cudaSuccess) {
+    cudaFree(ws);
+    delete h;
+    return cuda_fail(e, "zero_opt_create");
+  }
+  h->has_device = true;
+  *out = h;
+  return ZERO_OK;
+}
+
+zero_status zero_opt_destroy(zero_opt_t h) {
+  if (!h) return ZERO_OK;
+  if (h->has_device) {
+    int prev = -1;
+    cudaGetDevice(&prev);
+    cudaSetDevice(h->device);
+    cudaDeviceSynchronize();
+    for (Plan* p : h->plans) {
+      if (p->dev) cudaFree(p->dev);
+      delete p;
+    }
+    cudaFree(h->ws);
+    cudaFreeHost(h->pinned);
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+  delete h;
+  return ZERO_OK;
+}
+
+zero_status zero_opt_shard_bounds(zero_opt_t h, int32_t rank, int64_t* begin,
+                                  int64_t* real_end, int64_t* shard_len,
+                                  int64_t* padded_numel) {
+  zero_status st = check_handle_rank(h, rank);
+  if (st != ZERO_OK) return st;
+  int64_t b, e, s, p;
+  shard_of(h->cfg, rank, &b, &e, &s, &p);
+  if (begin) *begin = b;
+  if (real_end) *real_end = e;
+  if (shard_len) *shard_len = s;
+  if (padded_numel) *padded_numel = p;
+  return ZERO_OK;
+}
+
+zero_status zero_opt_memory_bytes(int64_t numel, int32_t world, int32_t stage,
+                                  int64_t* bytes) {
+  if (!bytes) return fail(ZERO_EINVAL, "bytes is NULL");
+  if (numel < 0 || world < 1) return fail(ZERO_EINVAL, "numel must be >= 0 and world >= 1");
+  if (stage < 0 || stage > 3) return fail(ZERO_ERANGE, "stage must be 0..3");
+  const int64_t S = (numel + world - 1) / world;
+  // 2 bytes of 16-bit parameters, 2 of 16-bit gradients, 12 of fp32 state.
+  const int64_t params = stage >= 3 ? 2 * S : 2 * numel;
+  const int64_t grads = stage >= 2 ? 2 * S : 2 * numel;
+  const int64_t state = stage >= 1 ? 12 * S : 12 * numel;
+  *bytes = params + grads + state;
+  return ZERO_OK;
+}
+
+zero_status zero_opt_grad_stats(zero_opt_t h, int32_t rank, const zero_opt_buffers* bufs,
+                                void* stream, zero_opt_stats* out) {
+  zero_status st = check_handle_rank(h, rank);
+  if (st != ZERO_OK) return st;
+  if (!out) return fail(ZERO_EINVAL, "out is NULL");
+  std::vector<HostRun> runs;
+  int nbuf = 0;
+  double divisor = 1.0;
+  st = flat_runs(h, rank, bufs, &runs, &nbuf, &divisor);
+  if (st != ZERO_OK) return st;
+  st = check_device(h);
+  if (st != ZERO_OK) return st;
+  st = run(h, rank, runs, nbuf, divisor, bufs->stash, stream, zo::kStatsOnly, nullptr);
+  if (st != ZERO_OK) return st;
+  struct {
+    double sumsq;
+    int32_t nonfinite;
+    int32_t pad;
+  } got;
+  st = read_small(h, &h->ws->own_sumsq, sizeof(got), stream, &got);
+  if (st != ZERO_OK) return st;
+  out->sumsq = got.sumsq;
+  out->nonfinite = got.nonfinite;
+  out->reserved = 0;
+  return ZERO_OK;
+}
+
+zero_status zero_opt_fold_stats(const zero_opt_stats* per_rank, int32_t n,
+                                zero_opt_stats* out) {
+  if (!out) return fail(ZERO_EINVAL, "out is NULL");
+  if (n < 0 || (n > 0 && !per_rank)) return fail(ZERO_EINVAL, "bad per-rank array");
+  double sumsq = 0.0;
+  int32_t nonfinite = 0;
+  for (int32_t r = 0; r < n; ++r) {
+    sumsq += per_rank[r].sumsq;
+    if (per_rank[r].nonfinite) nonfinite = 1;
+  }
+  out->sumsq = sumsq;
+  out->nonfinite = nonfinite;
+  out->reserved = 0;
+  return ZERO_OK;
+}
+
+zero_status zero_opt_step(zero_opt_t h, int32_t rank, const zero_opt_buffers* bufs,
+                          void* stream, const zero_opt_stats* global) {
+  zero_status st = check_handle_rank(h, rank);
+  if (st != ZERO_OK) return st;
+  std::vector<HostRun> runs;
+  int nbuf = 0;
+  double divisor = 1.0;
+  st = flat_runs(h, rank, bufs, &runs, &nbuf, &divisor);
+  if (st != ZERO_OK) return st;
+  st = check_device(h);
+  if (st != ZERO_OK) return st;
+  return run(h, rank, runs, nbuf, divisor, bufs->stash, stream,
+             global ? zo::kStepGlobal : zo::kStepLocal, global);
+}
+
+zero_status zero_opt_grad_stats_tensors(zero_opt_t h, int32_t rank,
+                                        const zero_opt_tensor_list* list, void* stream,
+                                        zero_opt_stats* out) {
+  zero_status st = check_handle_rank(h, rank);
+  if (st != ZERO_OK) return st;
+  if (!out) return fail(ZERO_EINVAL, "out is NULL");
+  std::vector<HostRun> runs;
+  int nbuf = 0;
+  double divisor = 1.0;
+  st = list_runs(list, &runs, &nbuf, &divisor);
+  if (st != ZERO_OK) return st;
+  st = check_device(h);
+  if (st != ZERO_OK) return st;
+  st = run(h, rank, runs, nbuf, divisor, list->stash, stream, zo::kStatsOnly, nullptr);
+  if (st != ZERO_OK) return st;
+  struct {
+    double sumsq;
+    int32_t nonfinite;
+    int32_t pad;
+  } got;
+  st = read_small(h, &h->ws->own_sumsq, sizeof(got), stream, &got);
+  if (st != ZERO_OK) return st;
+  out->sumsq = got.sumsq;
+  out->nonfinite = got.nonfinite;
+  out->reserved = 0;
+  return ZERO_OK;
+}
+
+zero_status zero_opt_step_tensors(zero_opt_t h, int32_t rank, const zero_opt_tensor_list* list,
+                                  void* stream, const zero_opt_stats* global) {
+  zero_status st = check_handle_rank(h, rank);
+  if (st != ZERO_OK) return st;
+  std::vector<HostRun> runs;
+  int nbuf = 0;
+  double divisor = 1.0;
+  st = list_runs(list, &runs, &nbuf, &divisor);
+  if (st != ZERO_OK) return st;
+  st = check_device(h);
+  if (st != ZERO_OK) return st;
+  return run(h, rank, runs, nbuf, divisor, list->stash, stream,
+             global ? zo::kStepGlobal : zo::kStepLocal, global);
+}
+
+zero_status zero_opt_loss_scale(zero_opt_t h, int32_t rank, void* stream,
+                                zero_opt_scaler_state* out) {
+  zero_status st = check_handle_rank(h, rank);
+  if (st != ZERO_OK) return st;
+  if (!out) return fail(ZERO_EINVAL, "out is NULL");
+  st = check_device(h);
+  if (st != ZERO_OK) return st;
+  return read_small(h, &h->ranks[rank], sizeof(zo::RankState), stream, out);
+}
+
+zero_status zero_opt_set_loss_scale(zero_opt_t h, int32_t rank, void* stream,
+                                    const zero_opt_scaler_state* in) {
+  zero_status st = check_handle_rank(h, rank);
+  if (st != ZERO_OK) return st;
+  if (!in) return fail(ZERO_EINVAL, "in is NULL");
+  if (!(in->scale > 0.0f) || in->clean_steps < 0 || in->t < 0 || in->skipped_total < 0)
+    return fail(ZERO_EINVAL, "scale must be > 0 and counters >= 0");
+  st = check_device(h);
+  if (st != ZERO_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Pageable source: staged before the call returns, ordered on the stream.
+  cudaError_t e = cudaMemcpyAsync(&h->ranks[rank], in, sizeof(zo::RankState),
+                                  cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
+  return ZERO_OK;
+}
+
+zero_status zero_opt_set_lr(zero_opt_t h, double lr) {
+  if (!h) return fail(ZERO_EINVAL, "handle is NULL");
+  if (!(lr >= 0.0)) return fail(ZERO_EINVAL, "lr must be >= 0");
+  h->cfg.lr = lr;
+  return ZERO_OK;
+}
+
+zero_status zero_opt_last_step(zero_opt_t h, void* stream, zero_opt_step_info* out) {
+  if (!h) return fail(ZERO_EINVAL, "handle is NULL");
+  if (!out) return fail(ZERO_EINVAL, "out is NULL");
+  zero_status st = check_device(h);
+  if (st != ZERO_OK) return st;
+  return read_small(h, &h->ws->dec, sizeof(zero_opt_step_info), stream, out);
+}
+
+zero_status zero_opt_set_events(zero_opt_t h, void* ev_start, void* ev_mid, void* ev_end) {
+  if (!h) return fail(ZERO_EINVAL, "handle is NULL");
+  h->ev[0] = static_cast<cudaEvent_t>(ev_start);
+  h->ev[1] = static_cast<cudaEvent_t>(ev_mid);
+  h->ev[2] = static_cast<cudaEvent_t>(ev_end);
+  return ZERO_OK;
+}
+
+zero_status zero_opt_launch_count(zero_opt_t h, int64_t* launches) {
+  if (!h || !launches) return fail(ZERO_EINVAL, "NULL argument");
+  *launches = h->launches;
+  return ZERO_OK;
+}
+
+const char* zero_opt_status_string(zero_status s) {
+  switch (s) {
+    case ZERO_OK: return "ZERO_OK";
+    case ZERO_EINVAL: return "ZERO_EINVAL: invalid argument";
+    case ZERO_ERANGE: return "ZERO_ERANGE: index or size out of range";
+    case ZERO_ENOMEM: return "ZERO_ENOMEM: allocation failed";
+    case ZERO_ECUDA: return "ZERO_ECUDA: CUDA error or no device";
+    case ZERO_ENOTSUP: return "ZERO_ENOTSUP: unsupported option";
+  }
+  return "unknown zero_status";
+}
+
+const char* zero_opt_last_error(void) { return g_err.c_str(); }
+
+}  // extern "C"

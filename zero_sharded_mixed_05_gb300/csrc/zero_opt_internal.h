@@ -1,0 +1,103 @@
+// zero_opt_internal.h -- device-visible data structures shared by the host
+// side (zero_opt.cu) and the kernels (kernels.cuh).  Not part of the ABI.
+#pragma once
+
+#include <stdint.h>
+
+#include "zero_opt.h"
+
+namespace zo {
+
+constexpr int kThreads = 256;            // threads per CTA
+constexpr int kVec = 8;                  // elements per thread per tile
+constexpr int kTile = kThreads * kVec;   // 2048 elements per tile
+constexpr int kMaxCtas = 4096;           // partial-sum slots in the workspace
+constexpr int kMaxBufs = 1024;           // R*K limit
+
+// One contiguous run of elements with its own buffers: the whole shard of a
+// flat buffer, or one tensor of a per-tensor list.  All pointers already point
+// at the run's first element.
+struct Seg {
+  float* master;
+  float* m;
+  float* v;
+  void* p16;
+  int64_t n;          // elements in the run (> 0)
+  int64_t tile0;      // first tile index of the run
+  int64_t ntiles;     // ceil(n / kTile)
+  int64_t stash_off;  // element offset of the run in the stash
+  int32_t gbase;      // first entry of the run's gradient pointers
+  int32_t vec;        // 1: every pointer 16-byte aligned (vector path)
+};
+
+// Loss-scaler replica of one rank; same layout as zero_opt_scaler_state.
+struct RankState {
+  float scale;
+  int32_t last_skipped;
+  int64_t clean;
+  int64_t t;
+  int64_t skipped_total;
+};
+static_assert(sizeof(RankState) == sizeof(zero_opt_scaler_state), "layout");
+
+// Decision of one step.  The first fields have the layout of
+// zero_opt_step_info; the binary32 scalars of the update follow.
+struct Decision {
+  double sumsq;
+  double norm;
+  float coef;
+  float scale_used;
+  int32_t skip;
+  int32_t nonfinite;
+  int64_t t;
+  float step_size, isb2, decay, b1, omb1, b2, omb2, eps;
+};
+static_assert(sizeof(zero_opt_step_info) <= sizeof(Decision), "layout");
+
+struct Workspace {
+  unsigned int ticket;   // CTAs of pass 1 that finished; reset by the last
+  int32_t pad0;
+  Decision dec;          // written by the last CTA of pass 1, read by pass 2
+  double own_sumsq;      // statistics-only result
+  int32_t own_nonfinite;
+  int32_t pad1;
+  double part_sumsq[kMaxCtas];
+  int32_t part_flag[kMaxCtas];
+};
+
+struct Hyper {
+  double lr, beta1, beta2, eps, wd, max_norm, divisor, min_scale, factor;
+  int64_t window;
+  int32_t bias_correction, dynamic;
+};
+
+enum Mode : int32_t { kStepLocal = 0, kStepGlobal = 1, kStatsOnly = 2 };
+
+struct Pass1Args {
+  const Seg* segs;
+  const void* const* gptrs;
+  int32_t nseg;
+  int32_t nbuf;
+  int64_t ntiles;        // 0: decide only
+  float* stash;          // non-NULL: store the reduced sums
+  int32_t mode;
+  int32_t rank;
+  double g_sumsq;        // kStepGlobal: the folded statistics
+  int32_t g_nonfinite;
+  int32_t pad;
+  Hyper hp;
+  Workspace* ws;
+  RankState* ranks;
+};
+
+struct Pass2Args {
+  const Seg* segs;
+  const void* const* gptrs;
+  int32_t nseg;
+  int32_t nbuf;
+  int64_t ntiles;
+  const float* stash;    // non-NULL: read the reduced sums from here
+  const Decision* dec;
+};
+
+}  // namespace zo
