@@ -229,6 +229,15 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- arms
 
+def max_over_ranks(value: float, device) -> float:
+    """Largest value over the ranks of the default process group."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -372,9 +381,7 @@ def run_ours(args):
     p1 = [evs[i][0].elapsed_time(evs[i][1]) for i in range(K)]
     p2 = [evs[i][1].elapsed_time(evs[i][2]) for i in range(K)]
     if ws > 1:
-        t = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+        ms_total = max_over_ranks(ms_total, dev)
     ms_step = ms_total / K
     n = setup.n
     value = ws * n / (ms_step * 1e-3)
@@ -413,9 +420,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / Ke
     if ws > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(e2e_ms, dev)
     e2e_value = ws * n / (e2e_ms * 1e-3)
 
     cpu = None
@@ -464,9 +469,18 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gpt2")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--numel", type=int, default=0,
+                    help="override the flat workload's parameters per shard (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.numel:
+        if args.workload == "pertensor":
+            ap.error("--numel applies to flat workloads")
+        w = dict(WORKLOADS[args.workload])
+        w["numel"] = args.numel * w["world"]
+        w["desc"] = w["desc"] + f" [resized to {args.numel:,} params per shard]"
+        WORKLOADS[args.workload] = w
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

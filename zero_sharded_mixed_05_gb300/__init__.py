@@ -351,3 +351,20 @@ def zero_opt_fold_stats(per_rank) -> zero_opt_stats:
     _check(lib().zero_opt_fold_stats(arr, len(per_rank), ctypes.byref(out)),
            "zero_opt_fold_stats")
     return out
+
+
+def allgather_fold(own: zero_opt_stats, group=None) -> zero_opt_stats:
+    """The scalar all-reduce of a multi-process run: every rank contributes its
+    shard's statistics, all ranks receive all of them (torch.distributed
+    all_gather on a tiny tensor) and fold them in rank order with
+    zero_opt_fold_stats, so every rank gets bit-identical totals."""
+    import torch
+    import torch.distributed as dist
+    ws = dist.get_world_size(group)
+    mine = torch.tensor([own.sumsq, float(own.nonfinite)], dtype=torch.float64)
+    if dist.get_backend(group) == "nccl":
+        mine = mine.cuda()
+    parts = [torch.empty_like(mine) for _ in range(ws)]
+    dist.all_gather(parts, mine, group=group)
+    per = [zero_opt_stats(float(p[0]), int(p[1]), 0) for p in (q.cpu() for q in parts)]
+    return zero_opt_fold_stats(per)
