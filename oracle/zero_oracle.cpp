@@ -162,17 +162,26 @@ extern "C" void orc_reduce(const uint16_t* const* bufs, int32_t nbuf, int64_t n,
 
 /* a2, a3: overflow flag and the sum of squares for the L2 norm.  The loss
  * scaler watches for gradients that overflowed to infinity ([CSDN] §2.2);
- * NaN counts as overflow too.  Each square is exact in binary64 (a binary32
- * product needs 48 significand bits); the sum is sequential in binary64. */
+ * NaN counts as overflow too.  The norm is a plain sum with no order, so the
+ * oracle computes the sum of squares to within one binary64 rounding of the
+ * exact value: each square is exact in binary64 (a binary32 product needs 48
+ * significand bits) and the running sum carries Neumaier's compensation term
+ * (A. Neumaier, "Rundungsfehleranalyse einiger Verfahren zur Summation
+ * endlicher Summen", ZAMM 54, 1974). */
 extern "C" orc_stats orc_stats_of(const float* s, int64_t n) {
   orc_stats st;
-  st.sumsq = 0.0;
   st.nonfinite = 0;
   st.pad_ = 0;
+  double sum = 0.0, comp = 0.0;
   for (int64_t j = 0; j < n; ++j) {
     if (!std::isfinite(s[j])) st.nonfinite = 1;
-    st.sumsq += (double)s[j] * (double)s[j];
+    const double x = (double)s[j] * (double)s[j];
+    const double t = sum + x;
+    if (std::fabs(sum) >= std::fabs(x)) comp += (sum - t) + x;
+    else comp += (x - t) + sum;
+    sum = t;
   }
+  st.sumsq = sum + comp;
   return st;
 }
 

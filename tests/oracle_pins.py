@@ -549,4 +549,22 @@ def pin_global_overflow_across_shards(orc):
         assert d.skip == 1 and (master == 1.0).all() and st.scale == 8.0, r
 
 
+
+
+def pin_sum_of_squares_is_correctly_rounded(orc):
+    """The sum of squares equals math.fsum (the correctly rounded sum) of the
+    exact binary64 squares, to within one ulp, for sums with a wide dynamic
+    range and many terms."""
+    import math
+    rng = np.random.default_rng(8)
+    for n, spread in [(10_000, 2), (200_000, 30), (3, 60)]:
+        s = (rng.standard_normal(n) * 2.0 ** rng.integers(-spread, spread, n)).astype(np.float32)
+        got = orc.stats_of(s).sumsq
+        ref = math.fsum((s.astype(np.float64) ** 2).tolist())
+        assert abs(got - ref) <= math.ulp(ref), (n, got, ref)
+    # a case where plain sequential binary64 summation loses the small terms
+    s = np.array([2.0 ** 30] + [2.0 ** -1] * 4096, np.float32)
+    assert orc.stats_of(s).sumsq == 2.0 ** 60 + 4096 * 0.25
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -1,0 +1,150 @@
+"""Full-size parity: the workloads at their full sizes, in the launch
+configuration bench.py times, checked on sampled outputs.
+
+The oracle computes each step's global statistics exactly over the whole
+gradient buffers (copied to the host in chunks), takes its own decisions and
+updates the sampled elements one by one; the GPU's outputs at those indices
+must match (fp32 state 1e-6 relative, abs 1e-9; 16-bit copy 1 ulp; norm 1e-5;
+skip and scale bit-exact).  An overflow is injected on the second step.
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+from harness import assert_state, to_np16, ulp16_diff
+
+pytestmark = pytest.mark.gpu
+
+CHUNK = 1 << 25
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+
+
+def _sample(n, seed, count):
+    rng = np.random.default_rng(seed)
+    tiles = np.arange(1, 50) * 2048
+    parts = [rng.integers(0, n, count), np.arange(min(n, 4096)),
+             np.arange(max(0, n - 4096), n), tiles - 1, tiles, tiles + 1]
+    idx = np.unique(np.concatenate(parts))
+    return idx[(idx >= 0) & (idx < n)]
+
+
+def _chunk_stats(orc, grads, code, c0, c1):
+    return orc.stats_of(orc.reduce([to_np16(g[c0:c1]) for g in grads], code))
+
+
+class Run:
+    """A workload as bench.Setup builds it, plus the oracle's view of a sample."""
+
+    def __init__(self, name):
+        import torch
+
+        import bench
+        self.torch = torch
+        self.s = bench.Setup(name, torch.device("cuda:0"))
+        w = self.s.w
+        self.code = O.FP16 if w["dtype"] == "fp16" else O.BF16
+        self.nb = w["R"] * w["K"]
+        self.hp = O.hparams(lr=w["lr"], weight_decay=w["wd"], max_grad_norm=w["clip"],
+                            dynamic_scale=w["dynamic"], scale_window=1000)
+        self.sc = O.scaler(w["scale"])
+        self.orc = O.default()
+        if name == "pertensor":
+            self.groups = [(it["master"], it["m"], it["v"], it["param16"], it["grads"])
+                           for it in self.s.items]
+        else:
+            self.groups = [(self.s.master, self.s.m, self.s.v, self.s.p16[0], self.s.grads)]
+        # the oracle's statistics of every chunk of every group, in list order;
+        # the gradients do not change between steps except for the injection
+        self.chunks = []
+        for gi, (master, _, _, _, grads) in enumerate(self.groups):
+            n = master.numel()
+            for c0 in range(0, n, CHUNK):
+                c1 = min(n, c0 + CHUNK)
+                self.chunks.append((gi, c0, c1, _chunk_stats(self.orc, grads, self.code, c0, c1)))
+        self.samples = []
+        for gi, (master, m, v, _, _) in enumerate(self.groups):
+            n = master.numel()
+            idx = _sample(n, 1000 + gi, 60_000 if len(self.groups) == 1 else 2_000)
+            ti = torch.from_numpy(idx).cuda()
+            self.samples.append(dict(ti=ti, master=master[ti].cpu().numpy().copy(),
+                                     m=m[ti].cpu().numpy().copy(),
+                                     v=v[ti].cpu().numpy().copy(),
+                                     p16=np.zeros(idx.size, np.uint16)))
+
+    def step(self, inject=None):
+        """One GPU step and the oracle on the sample."""
+        import zero_sharded_mixed_05_gb300 as z
+        saved = None
+        if inject is not None:
+            gi, j = inject
+            g = self.groups[gi][4][0]
+            saved = g[j].clone()
+            g[j] = float("inf")
+        per = []
+        for gi, c0, c1, st in self.chunks:
+            if inject is not None and gi == inject[0] and c0 <= inject[1] < c1:
+                st = _chunk_stats(self.orc, self.groups[gi][4], self.code, c0, c1)
+            per.append(st)
+        G = self.orc.fold_stats(per)
+        self.s.step()
+        info = z.zero_opt_last_step(self.s.h)
+        d = self.orc.decide(self.hp, self.sc, G, float(self.nb))
+        for smp, (_, _, _, _, grads) in zip(self.samples, self.groups):
+            s = self.orc.reduce([to_np16(g[smp["ti"]]) for g in grads], self.code)
+            self.orc.update(d, s, smp["master"], smp["m"], smp["v"], smp["p16"], self.code)
+        if saved is not None:
+            self.groups[inject[0]][4][0][inject[1]] = saved
+        self.torch.cuda.synchronize()
+        return info, d, G
+
+    def check(self):
+        for smp, (master, m, v, p16, _) in zip(self.samples, self.groups):
+            ti = smp["ti"]
+            assert_state("master", master[ti].cpu().numpy(), smp["master"])
+            assert_state("m", m[ti].cpu().numpy(), smp["m"])
+            assert_state("v", v[ti].cpu().numpy(), smp["v"])
+            assert ulp16_diff(to_np16(p16[ti]), smp["p16"]) <= 1
+
+
+def _run(name, steps=3, inject_step=2):
+    import zero_sharded_mixed_05_gb300 as z
+    run = Run(name)
+    try:
+        for step in range(1, steps + 1):
+            inject = (0, 12_345) if step == inject_step else None
+            info, d, G = run.step(inject)
+            assert info.skipped == d.skip == (1 if step == inject_step else 0)
+            assert info.scale_used == d.scale_used
+            assert info.t == run.sc.t
+            if not d.skip:
+                assert abs(info.norm - d.norm) <= 1e-5 * d.norm
+                assert abs(info.sumsq - G.sumsq) <= 1e-5 * G.sumsq
+            assert z.zero_opt_loss_scale(run.s.h, 0).as_tuple() == run.sc.as_tuple()
+            run.check()
+    finally:
+        z.zero_opt_destroy(run.s.h)
+
+
+def test_fullsize_gpt2():
+    _run("gpt2")
+
+
+def test_fullsize_llama_zero2_shard():
+    _run("llama")
+
+
+def test_fullsize_fused_reduce():
+    _run("fused")
+
+
+def test_fullsize_per_tensor_list():
+    _run("pertensor")

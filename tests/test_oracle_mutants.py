@@ -86,3 +86,15 @@ def test_mutant_is_caught(mutant_libs, idx):
     orc = oracle.Oracle(mutant_libs[idx])
     caught = _caught(orc)
     assert caught is not None, f"no pin detects the planted mistake: {MUTANTS[idx][0]}"
+
+
+def test_sum_of_squares_compensation_mutant_is_caught(tmp_path):
+    """Dropping the compensation (plain sequential binary64 summation) is
+    caught by the correctly-rounded pin."""
+    src = open(oracle.SOURCE).read()
+    old = "st.sumsq = sum + comp;"
+    assert src.count(old) == 1
+    path = tmp_path / "mut_sumsq.cpp"
+    path.write_text(src.replace(old, "st.sumsq = sum;"))
+    lib = oracle.compile_source(str(path), str(tmp_path / "libmuts.so"))
+    assert _caught(oracle.Oracle(lib)) is not None

@@ -32,6 +32,15 @@
 
 #include "zero_opt_internal.h"
 
+// Resident CTAs per SM each kernel is compiled for (register budget 65536 /
+// (256 * n) per thread).
+#ifndef ZO_PASS1_MIN_CTAS
+#define ZO_PASS1_MIN_CTAS 4
+#endif
+#ifndef ZO_PASS2_MIN_CTAS
+#define ZO_PASS2_MIN_CTAS 4
+#endif
+
 namespace zo {
 
 // ------------------------------------------------------------- 16-bit formats
@@ -119,43 +128,63 @@ __device__ __forceinline__ const unsigned short* grad_ptr(const void* const* gpt
   return reinterpret_cast<const unsigned short*>(raw);
 }
 
+// ------------------------------------------------------------- packed fp32x2
+// Blackwell issues two binary32 lanes per instruction (FADD2/FMUL2/FFMA2);
+// each lane rounds exactly like the scalar IEEE _rn operation.
+__device__ __forceinline__ float2 neg2(float2 a) { return make_float2(-a.x, -a.y); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) { return __fadd2_rn(a, neg2(b)); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+
 // ------------------------------------------------------------- sum of squares
-// Per tile the eight squares are accumulated in binary32 with fused
-// multiply-add; the tile partials are summed per thread with Kahan
-// compensation, and hi - c is taken in binary64 at the end, so the thread's
-// total is accurate to about one binary32 rounding per tile partial.  Tiles
-// holding a value of magnitude >= 2^50 (squares near the binary32 overflow
-// range, or inf/NaN) or whose squares all lie below 2^-80 (near underflow) are
-// summed in binary64 instead.  amax (largest |s| bit pattern) gives the
-// overflow flag: inf and NaN patterns are >= 0x7f800000.
+// The global norm needs the sum of squares of the reduced gradients to well
+// below binary32 precision (the clip coefficient is rounded to binary32 from
+// it), but GB300's binary64 rate is far too low for a binary64 operation per
+// element.  Each square is therefore formed exactly as p + e (p = s*s rounded,
+// e = fma(s, s, -p)) and added into a per-thread double-binary32 accumulator
+// (hi, lo) with Knuth's TwoSum, two lanes at a time; the thread's total
+// hi + lo is then taken in binary64.  The accumulated error is a few units of
+// 2^-48 of the thread's sum.  Tiles whose largest |s| is 2^50 or more (squares
+// near the binary32 overflow range, or inf/NaN), or whose values are all
+// nonzero and below 2^-40 (squares near underflow), are summed in binary64
+// instead.  amax (the largest |s| bit pattern seen) gives the overflow flag:
+// inf and NaN patterns are >= 0x7f800000.
 struct SqAcc {
-  float hi = 0.0f, c = 0.0f;
+  float2 hi = make_float2(0.0f, 0.0f);
+  float2 lo = make_float2(0.0f, 0.0f);
   double slow = 0.0;
   uint32_t amax = 0u;
 
   __device__ __forceinline__ void add(const float (&s)[kVec]) {
     uint32_t tmax = 0u;
-    float q = 0.0f;
 #pragma unroll
-    for (int i = 0; i < kVec; ++i) {
-      tmax = max(tmax, __float_as_uint(s[i]) & 0x7fffffffu);
-      q = __fmaf_rn(s[i], s[i], q);
-    }
+    for (int i = 0; i < kVec; ++i) tmax = max(tmax, __float_as_uint(s[i]) & 0x7fffffffu);
     amax = max(amax, tmax);
-    if (tmax >= 0x58800000u || (q < 0x1p-80f && tmax != 0u)) {
+    const bool fast = tmax < 0x58800000u && (tmax >= 0x2B800000u || tmax == 0u);
+    if (fast) {
+#pragma unroll
+      for (int i = 0; i < kVec / 2; ++i) {
+        const float2 x = make_float2(s[2 * i], s[2 * i + 1]);
+        const float2 p = mul2(x, x);
+        const float2 e = __ffma2_rn(x, x, neg2(p));
+        const float2 t = add2(hi, p);
+        const float2 bp = sub2(t, hi);
+        const float2 ap = sub2(t, bp);
+        const float2 err = add2(sub2(hi, ap), sub2(p, bp));
+        lo = add2(lo, add2(err, e));
+        hi = t;
+      }
+    } else {
       double d = 0.0;
 #pragma unroll
       for (int i = 0; i < kVec; ++i) d = __dadd_rn(d, __dmul_rn((double)s[i], (double)s[i]));
       slow = __dadd_rn(slow, d);
-    } else {
-      const float y = __fsub_rn(q, c);
-      const float t = __fadd_rn(hi, y);
-      c = __fsub_rn(__fsub_rn(t, hi), y);
-      hi = t;
     }
   }
   __device__ __forceinline__ double total() const {
-    return __dadd_rn(__dsub_rn((double)hi, (double)c), slow);
+    const double a = __dadd_rn((double)hi.x, (double)lo.x);
+    const double b = __dadd_rn((double)hi.y, (double)lo.y);
+    return __dadd_rn(__dadd_rn(a, b), slow);
   }
 };
 
@@ -253,7 +282,7 @@ __device__ void decide(const Pass1Args& a, double own_sumsq, int own_flag) {
 // reduced so that each thread keeps four 16-byte loads in flight.
 // NB == 0: any number of buffers, loaded in batches of eight per tile.
 template <typename GT, bool STASH, int NB>
-__global__ void __launch_bounds__(kThreads, 4) pass1_kernel(const Pass1Args a) {
+__global__ void __launch_bounds__(kThreads, ZO_PASS1_MIN_CTAS) pass1_kernel(const Pass1Args a) {
   __shared__ double red[kThreads / 32];
   __shared__ int s_last;
   constexpr int U = (NB == 1) ? 4 : 1;
@@ -383,13 +412,27 @@ __device__ __forceinline__ void adam_elem(float sj, float& p, float& m, float& v
   p = __fsub_rn(p, __fmul_rn(c.step_size, __fdiv_rn(m, den)));
 }
 
+// The same sequence on two elements at once with packed fp32x2 arithmetic
+// (identical rounding per lane); square root and division stay scalar.
+__device__ __forceinline__ void adam_pair(float2 s, float2& p, float2& m, float2& v,
+                                          const Scalars& c) {
+  const float2 g = mul2(s, make_float2(c.coef, c.coef));
+  m = add2(mul2(make_float2(c.b1, c.b1), m), mul2(make_float2(c.omb1, c.omb1), g));
+  v = add2(mul2(make_float2(c.b2, c.b2), v), mul2(make_float2(c.omb2, c.omb2), mul2(g, g)));
+  const float2 r = make_float2(__fsqrt_rn(v.x), __fsqrt_rn(v.y));
+  const float2 den = add2(mul2(r, make_float2(c.isb2, c.isb2)), make_float2(c.eps, c.eps));
+  p = mul2(p, make_float2(c.decay, c.decay));
+  const float2 q = make_float2(__fdiv_rn(m.x, den.x), __fdiv_rn(m.y, den.y));
+  p = sub2(p, mul2(make_float2(c.step_size, c.step_size), q));
+}
+
 __device__ __forceinline__ void f4_to(const float4& a, float* d) {
   d[0] = a.x; d[1] = a.y; d[2] = a.z; d[3] = a.w;
 }
 
 // SRC == 1: one gradient buffer; SRC == 0: a.nbuf buffers; SRC == -1: stash.
 template <typename GT, typename PT, int SRC>
-__global__ void __launch_bounds__(kThreads, 4) pass2_kernel(const Pass2Args a) {
+__global__ void __launch_bounds__(kThreads, ZO_PASS2_MIN_CTAS) pass2_kernel(const Pass2Args a) {
   const Decision* dp = a.dec;
   if (dp->skip) return;
   Scalars c;
@@ -453,7 +496,18 @@ __global__ void __launch_bounds__(kThreads, 4) pass2_kernel(const Pass2Args a) {
       f4_to(__ldcs(vm), v);
       f4_to(__ldcs(vm + 1), v + 4);
 #pragma unroll
-      for (int i = 0; i < kVec; ++i) adam_elem(x[i], p[i], m[i], v[i], c);
+      for (int i = 0; i < kVec / 2; ++i) {
+        float2 pp = make_float2(p[2 * i], p[2 * i + 1]);
+        float2 mm2 = make_float2(m[2 * i], m[2 * i + 1]);
+        float2 vv = make_float2(v[2 * i], v[2 * i + 1]);
+        adam_pair(make_float2(x[2 * i], x[2 * i + 1]), pp, mm2, vv, c);
+        p[2 * i] = pp.x;
+        p[2 * i + 1] = pp.y;
+        m[2 * i] = mm2.x;
+        m[2 * i + 1] = mm2.y;
+        v[2 * i] = vv.x;
+        v[2 * i + 1] = vv.y;
+      }
       float4* po = reinterpret_cast<float4*>(s.master + e0);
       float4* mo = reinterpret_cast<float4*>(s.m + e0);
       float4* vo = reinterpret_cast<float4*>(s.v + e0);
