@@ -293,6 +293,69 @@ zero_status zero_opt_set_events(zero_opt_t h, void* ev_start, void* ev_mid, void
 /* Kernels launched by this handle since creation (for launch accounting). */
 zero_status zero_opt_launch_count(zero_opt_t h, int64_t* launches);
 
+/* ---------------------------------------------------------------------------
+ * Sharded checkpoints.  A DeepSpeed engine saves one checkpoint per rank and
+ * resumes from it under the same world size and stage; zero_to_fp32.py merges
+ * the ZeRO shards into one full fp32 state dict ("DeepSpeed framework
+ * interview answer" (algomooc.com), "训练与恢复边界").
+ *
+ * File format (little-endian): 8-byte magic "ZOPTSHD1", uint32 version (1),
+ * uint32 reserved (0), the fields of zero_opt_ckpt_info in declaration order
+ * (int64 numel, int32 world, int32 rank, int64 begin, int64 real_len, then
+ * float scale, int32 last_skipped, int64 clean_steps, int64 t, int64
+ * skipped_total), uint64 checksum of the payload, then the payload: real_len
+ * fp32 master weights, real_len fp32 m, real_len fp32 v.  Padding is not
+ * stored.  The checksum is 64-bit FNV-1a over the payload taken as 8-byte
+ * little-endian words (a trailing partial word zero-extended).
+ * ------------------------------------------------------------------------- */
+typedef struct zero_opt_ckpt_info {
+  int64_t numel;            /* Ψ of the flat buffer                           */
+  int32_t world;            /* N                                              */
+  int32_t rank;             /* rank whose shard this is                       */
+  int64_t begin;            /* first flat index of the shard (rank * S)       */
+  int64_t real_len;         /* real elements stored (no padding)              */
+  zero_opt_scaler_state scaler;
+} zero_opt_ckpt_info;
+
+/* Write one shard file from HOST arrays of info->real_len floats each.
+ * Errors: EINVAL (NULL arguments; info not describing rank's shard of numel
+ * over world; an I/O failure, with the system error in zero_opt_last_error()). */
+zero_status zero_opt_ckpt_write(const char* path, const zero_opt_ckpt_info* info,
+                                const float* master, const float* m, const float* v);
+
+/* Read a shard file's header into *info and, for each non-NULL HOST array of
+ * info->real_len floats, its payload; the checksum is verified whenever the
+ * payload is read.  Errors: EINVAL (NULL path/info, unreadable file, bad magic
+ * or version, size not matching the header, checksum mismatch). */
+zero_status zero_opt_ckpt_read(const char* path, zero_opt_ckpt_info* info,
+                               float* master, float* m, float* v);
+
+/* Save `rank`'s shard: its DEVICE master, m and v (shard-local; the first
+ * real_len elements are stored) and its loss-scaler replica.  Synchronizes
+ * `stream`.  Errors: as zero_opt_ckpt_write, plus ERANGE (rank), ECUDA. */
+zero_status zero_opt_save_shard(zero_opt_t h, int32_t rank, const float* master,
+                                const float* m, const float* v, void* stream,
+                                const char* path);
+
+/* Resume `rank`'s shard from a file written for the same numel, world and
+ * rank: fills the DEVICE master, m and v (shard-local), restores the rank's
+ * loss-scaler replica and, when param16 is non-NULL, rewrites the rank's
+ * slice of the 16-bit parameter copy as the rounding of the restored master
+ * weights (param16 is the full padded buffer unless param16_shard_local).
+ * Synchronizes `stream`.  Errors: EINVAL (file for another numel/world/rank,
+ * unreadable or corrupt file), ERANGE, ECUDA. */
+zero_status zero_opt_load_shard(zero_opt_t h, int32_t rank, float* master, float* m,
+                                float* v, void* param16, int32_t param16_shard_local,
+                                void* stream, const char* path);
+
+/* zero_to_fp32: merge the shard files of one checkpoint (n_paths == world, in
+ * any order) into the full fp32 master weights out[0..numel) (HOST), padding
+ * dropped.  Every rank must appear exactly once and all files must agree on
+ * numel and world.  Host only.  Errors: EINVAL (NULL, unreadable or corrupt
+ * file, missing or duplicate rank, numel or world mismatch). */
+zero_status zero_opt_consolidate_fp32(const char* const* paths, int32_t n_paths,
+                                      int64_t numel, float* out);
+
 /* Static string describing a status code; never NULL. */
 const char* zero_opt_status_string(zero_status s);
 

@@ -153,6 +153,7 @@ class Oracle:
                                ctypes.POINTER(Stats), ctypes.POINTER(Stats),
                                ctypes.POINTER(Decision)]
         L.orc_step.restype = ctypes.c_int
+        L.orc_consolidate.argtypes = [_P, _I32, _I64, _P]
         self.L = L
         self.path = path
 
@@ -237,6 +238,15 @@ class Oracle:
         return own, dec
 
 
+    def consolidate(self, shard_masters, numel: int) -> np.ndarray:
+        """Full fp32 weights from the N shards' master arrays (rank order)."""
+        arrs = [np.ascontiguousarray(a, np.float32) for a in shard_masters]
+        ptrs = _ptr_array(arrs)
+        out = np.empty(numel, np.float32)
+        self.L.orc_consolidate(ctypes.cast(ptrs, _P), len(arrs), numel, _ptr(out))
+        return out
+
+
 _default: Oracle | None = None
 
 
@@ -251,6 +261,7 @@ def default() -> Oracle:
 def __getattr__(name):
     # Module-level shortcuts: oracle.step(...), oracle.shard_bounds(...), ...
     if name in ("shard_bounds", "memory_bytes", "f32_to_16", "f16_to_f32",
-                "reduce", "stats_of", "fold_stats", "decide", "update", "step"):
+                "reduce", "stats_of", "fold_stats", "decide", "update", "step",
+                "consolidate"):
         return getattr(default(), name)
     raise AttributeError(name)

@@ -311,3 +311,14 @@ extern "C" int orc_step(const orc_hparams* hp, orc_scaler* st,
   delete[] s;
   return 0;
 }
+
+/* zero_to_fp32 ("DeepSpeed framework interview answer", "训练与恢复边界"):
+ * merge the ZeRO shards into one full fp32 state, padding dropped. */
+extern "C" void orc_consolidate(const float* const* shard_master, int32_t world,
+                                int64_t numel, float* out) {
+  for (int32_t r = 0; r < world; ++r) {
+    int64_t b[4];
+    orc_shard_bounds(numel, world, r, b);
+    for (int64_t j = b[0]; j < b[1]; ++j) out[j] = shard_master[r][j - b[0]];
+  }
+}

@@ -118,6 +118,11 @@ int orc_step(const orc_hparams* hp, orc_scaler* st,
              float* master, float* m, float* v, uint16_t* p16, int32_t pdtype,
              const orc_stats* global, orc_stats* own, orc_decision* dec);
 
+/* zero_to_fp32: the full fp32 weights are the real parts of the N shards'
+ * master weights laid end to end in rank order, padding dropped. */
+void orc_consolidate(const float* const* shard_master, int32_t world, int64_t numel,
+                     float* out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -567,4 +567,28 @@ def pin_sum_of_squares_is_correctly_rounded(orc):
     assert orc.stats_of(s).sumsq == 2.0 ** 60 + 4096 * 0.25
 
 
+
+
+def pin_consolidation_is_the_unsharded_state(orc):
+    """zero_to_fp32 of a sharded run equals the master weights of the same run
+    done unsharded; padding never appears in the result."""
+    numel, N = 1001, 4
+    grads = [synth.normal_np(21, 1 + r, 0, numel, 8.0, synth.F16) for r in range(2)]
+    p0 = synth.normal_np(21, 0, 0, numel, 0.02, synth.F32)
+    hp = O.hparams(lr=1e-3)
+    ref = _state(numel, p0)
+    orc.step(hp, O.scaler(4.0), grads, F16, *ref, F16, 2.0)
+    bounds = [orc.shard_bounds(numel, N, r) for r in range(N)]
+    G = orc.fold_stats([orc.stats_of(orc.reduce([g[b:e].copy() for g in grads], F16))
+                        for b, e, _, _ in bounds])
+    shards = []
+    for b, e, _, _ in bounds:
+        st = _state(e - b, p0[b:e])
+        orc.step(hp, O.scaler(4.0), [g[b:e].copy() for g in grads], F16, *st, F16, 2.0, G)
+        shards.append(st[0])
+    full = orc.consolidate(shards, numel)
+    assert full.size == numel
+    assert (full.view(np.uint32) == ref[0].view(np.uint32)).all()
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -98,3 +98,15 @@ def test_sum_of_squares_compensation_mutant_is_caught(tmp_path):
     path.write_text(src.replace(old, "st.sumsq = sum;"))
     lib = oracle.compile_source(str(path), str(tmp_path / "libmuts.so"))
     assert _caught(oracle.Oracle(lib)) is not None
+
+
+def test_consolidation_mutant_is_caught(tmp_path):
+    src = open(oracle.SOURCE).read()
+    old = "for (int64_t j = b[0]; j < b[1]; ++j) out[j] = shard_master[r][j - b[0]];"
+    new = ("for (int64_t j = b[0]; j < b[1]; ++j) "
+           "out[j] = shard_master[r][j - b[0] + (j + 1 < b[1] ? 1 : 0)];")
+    assert src.count(old) == 1
+    path = tmp_path / "mut_consolidate.cpp"
+    path.write_text(src.replace(old, new))
+    lib = oracle.compile_source(str(path), str(tmp_path / "libmutc.so"))
+    assert _caught(oracle.Oracle(lib)) is not None

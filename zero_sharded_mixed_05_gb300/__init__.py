@@ -73,6 +73,11 @@ class zero_opt_scaler_state(ctypes.Structure):
                 int(self.skipped_total), int(self.last_skipped))
 
 
+class zero_opt_ckpt_info(ctypes.Structure):
+    _fields_ = [("numel", _i64), ("world", _i32), ("rank", _i32), ("begin", _i64),
+                ("real_len", _i64), ("scaler", zero_opt_scaler_state)]
+
+
 class ZeroOptError(RuntimeError):
     def __init__(self, status: int, where: str, message: str):
         super().__init__(f"{where}: status {status}: {message}")
@@ -104,6 +109,11 @@ SIGNATURES = [
     ("zero_opt_last_step", _i32, [_vp, _vp, _P(zero_opt_step_info)]),
     ("zero_opt_set_events", _i32, [_vp, _vp, _vp, _vp]),
     ("zero_opt_launch_count", _i32, [_vp, _P(_i64)]),
+    ("zero_opt_ckpt_write", _i32, [ctypes.c_char_p, _P(zero_opt_ckpt_info), _vp, _vp, _vp]),
+    ("zero_opt_ckpt_read", _i32, [ctypes.c_char_p, _P(zero_opt_ckpt_info), _vp, _vp, _vp]),
+    ("zero_opt_save_shard", _i32, [_vp, _i32, _vp, _vp, _vp, _vp, ctypes.c_char_p]),
+    ("zero_opt_load_shard", _i32, [_vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp, ctypes.c_char_p]),
+    ("zero_opt_consolidate_fp32", _i32, [_P(ctypes.c_char_p), _i32, _i64, _vp]),
     ("zero_opt_status_string", ctypes.c_char_p, [_i32]),
     ("zero_opt_last_error", ctypes.c_char_p, []),
 ]
@@ -368,3 +378,54 @@ def allgather_fold(own: zero_opt_stats, group=None) -> zero_opt_stats:
     dist.all_gather(parts, mine, group=group)
     per = [zero_opt_stats(float(p[0]), int(p[1]), 0) for p in (q.cpu() for q in parts)]
     return zero_opt_fold_stats(per)
+
+
+# ---------------------------------------------------------------- checkpoints
+
+def _np_ptr(a):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"] and a.dtype.itemsize == 4
+    return a.ctypes.data
+
+
+def zero_opt_ckpt_write(path: str, info: zero_opt_ckpt_info, master, m, v) -> None:
+    """Write one shard file from host float32 numpy arrays."""
+    _check(lib().zero_opt_ckpt_write(os.fsencode(path), ctypes.byref(info), _np_ptr(master),
+                                     _np_ptr(m), _np_ptr(v)), "zero_opt_ckpt_write")
+
+
+def zero_opt_ckpt_read(path: str, with_payload: bool = True):
+    """(info, master, m, v) of a shard file, arrays as host numpy float32."""
+    import numpy as np
+    info = zero_opt_ckpt_info()
+    _check(lib().zero_opt_ckpt_read(os.fsencode(path), ctypes.byref(info), None, None, None),
+           "zero_opt_ckpt_read")
+    if not with_payload:
+        return info, None, None, None
+    arrs = [np.empty(info.real_len, np.float32) for _ in range(3)]
+    _check(lib().zero_opt_ckpt_read(os.fsencode(path), ctypes.byref(info),
+                                    *[_np_ptr(a) for a in arrs]), "zero_opt_ckpt_read")
+    return (info, *arrs)
+
+
+def zero_opt_save_shard(h, rank: int, master, m, v, path: str, stream=None) -> None:
+    _check(lib().zero_opt_save_shard(h, rank, _ptr(master), _ptr(m), _ptr(v), _stream(stream),
+                                     os.fsencode(path)), "zero_opt_save_shard")
+
+
+def zero_opt_load_shard(h, rank: int, master, m, v, path: str, param16=None,
+                        param16_shard_local: bool = False, stream=None) -> None:
+    _check(lib().zero_opt_load_shard(h, rank, _ptr(master), _ptr(m), _ptr(v), _ptr(param16),
+                                     int(param16_shard_local), _stream(stream),
+                                     os.fsencode(path)), "zero_opt_load_shard")
+
+
+def zero_opt_consolidate_fp32(paths, numel: int):
+    """Full fp32 master weights (numpy) merged from one checkpoint's shard files."""
+    import numpy as np
+    arr = (ctypes.c_char_p * len(paths))(*[os.fsencode(p) for p in paths])
+    out = np.empty(numel, np.float32)
+    _check(lib().zero_opt_consolidate_fp32(arr, len(paths), numel, _np_ptr(out)),
+           "zero_opt_consolidate_fp32")
+    return out

@@ -10,8 +10,9 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 INCLUDE = os.path.join(ROOT, "include")
 CSRC = os.path.join(PKG, "csrc")
-SOURCES = [os.path.join(CSRC, "zero_opt.cu")]
-DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("kernels.cuh", "zero_opt_internal.h")] + [
+SOURCES = [os.path.join(CSRC, "zero_opt.cu"), os.path.join(CSRC, "ckpt.cpp")]
+DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("kernels.cuh", "zero_opt_internal.h",
+                                                     "host_util.h")] + [
     os.path.join(INCLUDE, "zero_opt.h")]
 LIB = os.path.join(PKG, "libzero_opt.so")
 

@@ -543,4 +543,20 @@ __global__ void __launch_bounds__(kThreads, ZO_PASS2_MIN_CTAS) pass2_kernel(cons
   }
 }
 
+// ------------------------------------------------------------- 16-bit copy
+// Rewrite a 16-bit parameter slice as the rounding of fp32 master weights
+// (when a shard is restored from a checkpoint).
+struct CastArgs {
+  const float* master;
+  unsigned short* p16;
+  int64_t n;
+};
+
+template <typename PT>
+__global__ void __launch_bounds__(kThreads) cast_kernel(const CastArgs a) {
+  for (int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x; i < a.n;
+       i += (int64_t)gridDim.x * kThreads)
+    a.p16[i] = Fmt<PT>::enc(a.master[i]);
+}
+
 }  // namespace zo

@@ -19,12 +19,15 @@
 #include <string>
 #include <vector>
 
+#include "host_util.h"
 #include "kernels.cuh"
 #include "zero_opt.h"
 
 namespace {
-
 thread_local std::string g_err;
+}  // namespace
+
+namespace zo {
 
 zero_status fail(zero_status s, const char* fmt, ...) {
   char buf[512];
@@ -35,6 +38,23 @@ zero_status fail(zero_status s, const char* fmt, ...) {
   g_err = buf;
   return s;
 }
+
+void shard_range(int64_t numel, int32_t world, int32_t rank, int64_t* begin,
+                 int64_t* real_len, int64_t* shard_len) {
+  const int64_t S = (numel + world - 1) / world;
+  const int64_t b = (int64_t)rank * S;
+  int64_t e = std::min(b + S, numel);
+  if (e < b) e = b;
+  *begin = b;
+  *real_len = e - b;
+  *shard_len = S;
+}
+
+}  // namespace zo
+
+namespace {
+
+using zo::fail;
 
 zero_status cuda_fail(cudaError_t e, const char* what) {
   return fail(ZERO_ECUDA, "%s: %s", what, cudaGetErrorString(e));
@@ -719,6 +739,87 @@ zero_status zero_opt_last_step(zero_opt_t h, void* stream, zero_opt_step_info* o
   zero_status st = check_device(h);
   if (st != ZERO_OK) return st;
   return read_small(h, &h->ws->dec, sizeof(zero_opt_step_info), stream, out);
+}
+
+zero_status zero_opt_save_shard(zero_opt_t h, int32_t rank, const float* master,
+                                const float* m, const float* v, void* stream,
+                                const char* path) {
+  zero_status st = check_handle_rank(h, rank);
+  if (st != ZERO_OK) return st;
+  if (!path) return fail(ZERO_EINVAL, "path is NULL");
+  zero_opt_ckpt_info info;
+  std::memset(&info, 0, sizeof(info));
+  int64_t shard = 0;
+  zo::shard_range(h->cfg.numel, h->cfg.world, rank, &info.begin, &info.real_len, &shard);
+  info.numel = h->cfg.numel;
+  info.world = h->cfg.world;
+  info.rank = rank;
+  if (info.real_len > 0 && (!master || !m || !v))
+    return fail(ZERO_EINVAL, "master, m and v must be non-NULL");
+  st = check_device(h);
+  if (st != ZERO_OK) return st;
+  st = zero_opt_loss_scale(h, rank, stream, &info.scaler);
+  if (st != ZERO_OK) return st;
+  const size_t n = (size_t)info.real_len;
+  std::vector<float> hm(n), hmm(n), hv(n);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (n > 0) {
+    e = cudaMemcpyAsync(hm.data(), master, n * 4, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(hmm.data(), m, n * 4, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(hv.data(), v, n * 4, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "zero_opt_save_shard");
+  return zero_opt_ckpt_write(path, &info, hm.data(), hmm.data(), hv.data());
+}
+
+zero_status zero_opt_load_shard(zero_opt_t h, int32_t rank, float* master, float* m,
+                                float* v, void* param16, int32_t param16_shard_local,
+                                void* stream, const char* path) {
+  zero_status st = check_handle_rank(h, rank);
+  if (st != ZERO_OK) return st;
+  if (!path) return fail(ZERO_EINVAL, "path is NULL");
+  zero_opt_ckpt_info info;
+  st = zero_opt_ckpt_read(path, &info, nullptr, nullptr, nullptr);
+  if (st != ZERO_OK) return st;
+  if (info.numel != h->cfg.numel || info.world != h->cfg.world || info.rank != rank)
+    return fail(ZERO_EINVAL, "%s was written for numel %lld, world %d, rank %d", path,
+                (long long)info.numel, info.world, info.rank);
+  if (info.real_len > 0 && (!master || !m || !v))
+    return fail(ZERO_EINVAL, "master, m and v must be non-NULL");
+  st = check_device(h);
+  if (st != ZERO_OK) return st;
+  const size_t n = (size_t)info.real_len;
+  std::vector<float> hm(n), hmm(n), hv(n);
+  st = zero_opt_ckpt_read(path, &info, hm.data(), hmm.data(), hv.data());
+  if (st != ZERO_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (n > 0) {
+    e = cudaMemcpyAsync(master, hm.data(), n * 4, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(m, hmm.data(), n * 4, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(v, hv.data(), n * 4, cudaMemcpyHostToDevice, s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "zero_opt_load_shard");
+  st = zero_opt_set_loss_scale(h, rank, stream, &info.scaler);
+  if (st != ZERO_OK) return st;
+  if (param16 && n > 0) {
+    zo::CastArgs ca;
+    ca.master = master;
+    ca.p16 = static_cast<unsigned short*>(param16) + (param16_shard_local ? 0 : info.begin);
+    ca.n = (int64_t)n;
+    const void* fn = h->cfg.param_dtype == ZERO_FP16
+                         ? reinterpret_cast<const void*>(zo::cast_kernel<__half>)
+                         : reinterpret_cast<const void*>(zo::cast_kernel<__nv_bfloat16>);
+    const int64_t grid = std::max<int64_t>(
+        1, std::min<int64_t>((int64_t)h->sms * 8, ((int64_t)n + zo::kThreads - 1) / zo::kThreads));
+    st = launch_kernel(h, fn, (int)grid, &ca, s);
+    if (st != ZERO_OK) return st;
+  }
+  e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "zero_opt_load_shard");
+  return ZERO_OK;
 }
 
 zero_status zero_opt_set_events(zero_opt_t h, void* ev_start, void* ev_mid, void* ev_end) {
