@@ -38,7 +38,12 @@
 #define ZO_PASS1_MIN_CTAS 4
 #endif
 #ifndef ZO_PASS2_MIN_CTAS
-#define ZO_PASS2_MIN_CTAS 4
+#define ZO_PASS2_MIN_CTAS 2
+#endif
+// Tiles whose 16-byte gradient loads pass 1 issues before reducing any of
+// them, when there is a single gradient buffer.
+#ifndef ZO_PASS1_UNROLL
+#define ZO_PASS1_UNROLL 4
 #endif
 
 namespace zo {
@@ -128,33 +133,51 @@ __device__ __forceinline__ const unsigned short* grad_ptr(const void* const* gpt
   return reinterpret_cast<const unsigned short*>(raw);
 }
 
-// ------------------------------------------------------------- packed fp32x2
-// Blackwell issues two binary32 lanes per instruction (FADD2/FMUL2/FFMA2);
-// each lane rounds exactly like the scalar IEEE _rn operation.
-__device__ __forceinline__ float2 neg2(float2 a) { return make_float2(-a.x, -a.y); }
-__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
-__device__ __forceinline__ float2 sub2(float2 a, float2 b) { return __fadd2_rn(a, neg2(b)); }
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
-
 // ------------------------------------------------------------- sum of squares
 // The global norm needs the sum of squares of the reduced gradients to well
 // below binary32 precision (the clip coefficient is rounded to binary32 from
 // it), but GB300's binary64 rate is far too low for a binary64 operation per
 // element.  Each square is therefore formed exactly as p + e (p = s*s rounded,
 // e = fma(s, s, -p)) and added into a per-thread double-binary32 accumulator
-// (hi, lo) with Knuth's TwoSum, two lanes at a time; the thread's total
-// hi + lo is then taken in binary64.  The accumulated error is a few units of
-// 2^-48 of the thread's sum.  Tiles whose largest |s| is 2^50 or more (squares
-// near the binary32 overflow range, or inf/NaN), or whose values are all
-// nonzero and below 2^-40 (squares near underflow), are summed in binary64
-// instead.  amax (the largest |s| bit pattern seen) gives the overflow flag:
-// inf and NaN patterns are >= 0x7f800000.
+// (hi, lo) with Knuth's TwoSum; even and odd elements go to two independent
+// accumulators so consecutive additions do not wait on each other.  The
+// thread's total hi + lo is taken in binary64; the accumulated error is a few
+// units of 2^-48 of the thread's sum.  Every operation is an explicit IEEE
+// round-to-nearest intrinsic, so nothing is contracted.  Tiles whose largest
+// |s| is 2^50 or more (squares near the binary32 overflow range, or inf/NaN),
+// or whose values are all nonzero and below 2^-40 (squares near underflow),
+// are summed in binary64 instead.  amax (the largest |s| bit pattern seen)
+// gives the overflow flag: inf and NaN patterns are >= 0x7f800000.
 struct SqAcc {
-  float2 hi = make_float2(0.0f, 0.0f);
-  float2 lo = make_float2(0.0f, 0.0f);
+  float hi0 = 0.0f, lo0 = 0.0f, hi1 = 0.0f, lo1 = 0.0f;
   double slow = 0.0;
   uint32_t amax = 0u;
 
+  static __device__ __forceinline__ void two_sum_add(float& hi, float& lo, float x) {
+    const float p = __fmul_rn(x, x);
+    const float e = __fmaf_rn(x, x, -p);
+    const float t = __fadd_rn(hi, p);
+    const float bp = __fsub_rn(t, hi);
+    const float ap = __fsub_rn(t, bp);
+    const float err = __fadd_rn(__fsub_rn(hi, ap), __fsub_rn(p, bp));
+    lo = __fadd_rn(lo, __fadd_rn(err, e));
+    hi = t;
+  }
+
+  // Square known to be exact in binary32 (a 16-bit value in the fast range):
+  // TwoSum only.
+  static __device__ __forceinline__ void two_sum_add_exact(float& hi, float& lo, float x) {
+    const float p = __fmul_rn(x, x);
+    const float t = __fadd_rn(hi, p);
+    const float bp = __fsub_rn(t, hi);
+    const float ap = __fsub_rn(t, bp);
+    lo = __fadd_rn(lo, __fadd_rn(__fsub_rn(hi, ap), __fsub_rn(p, bp)));
+    hi = t;
+  }
+
+  // EXACT_SQ: every s is a converted 16-bit value, whose square (fp16: 22
+  // significant bits, bf16: 16) is exact in binary32 inside the fast range.
+  template <bool EXACT_SQ = false>
   __device__ __forceinline__ void add(const float (&s)[kVec]) {
     uint32_t tmax = 0u;
 #pragma unroll
@@ -163,16 +186,14 @@ struct SqAcc {
     const bool fast = tmax < 0x58800000u && (tmax >= 0x2B800000u || tmax == 0u);
     if (fast) {
 #pragma unroll
-      for (int i = 0; i < kVec / 2; ++i) {
-        const float2 x = make_float2(s[2 * i], s[2 * i + 1]);
-        const float2 p = mul2(x, x);
-        const float2 e = __ffma2_rn(x, x, neg2(p));
-        const float2 t = add2(hi, p);
-        const float2 bp = sub2(t, hi);
-        const float2 ap = sub2(t, bp);
-        const float2 err = add2(sub2(hi, ap), sub2(p, bp));
-        lo = add2(lo, add2(err, e));
-        hi = t;
+      for (int i = 0; i < kVec; i += 2) {
+        if (EXACT_SQ) {
+          two_sum_add_exact(hi0, lo0, s[i]);
+          two_sum_add_exact(hi1, lo1, s[i + 1]);
+        } else {
+          two_sum_add(hi0, lo0, s[i]);
+          two_sum_add(hi1, lo1, s[i + 1]);
+        }
       }
     } else {
       double d = 0.0;
@@ -182,8 +203,8 @@ struct SqAcc {
     }
   }
   __device__ __forceinline__ double total() const {
-    const double a = __dadd_rn((double)hi.x, (double)lo.x);
-    const double b = __dadd_rn((double)hi.y, (double)lo.y);
+    const double a = __dadd_rn((double)hi0, (double)lo0);
+    const double b = __dadd_rn((double)hi1, (double)lo1);
     return __dadd_rn(__dadd_rn(a, b), slow);
   }
 };
@@ -285,7 +306,7 @@ template <typename GT, bool STASH, int NB>
 __global__ void __launch_bounds__(kThreads, ZO_PASS1_MIN_CTAS) pass1_kernel(const Pass1Args a) {
   __shared__ double red[kThreads / 32];
   __shared__ int s_last;
-  constexpr int U = (NB == 1) ? 4 : 1;
+  constexpr int U = (NB == 1) ? ZO_PASS1_UNROLL : 1;
   const int tid = threadIdx.x;
   const int64_t G = gridDim.x;
   SqAcc acc;
@@ -320,9 +341,10 @@ __global__ void __launch_bounds__(kThreads, ZO_PASS1_MIN_CTAS) pass1_kernel(cons
       const bool vec = s.vec && e0 + kVec <= s.n;
       float x[kVec];
       if (NB == 1 && fast[u]) {
+        // one buffer: the sum is 0 + g, which differs from g only in the sign
+        // of a zero -- irrelevant to the statistics and never stored here
+        // (a single buffer is never stashed)
         Fmt<GT>::dec8(raw[u], x);
-#pragma unroll
-        for (int i = 0; i < kVec; ++i) x[i] = __fadd_rn(0.0f, x[i]);
       } else if (NB != 1 && vec) {
 #pragma unroll
         for (int i = 0; i < kVec; ++i) x[i] = 0.0f;
@@ -367,7 +389,8 @@ __global__ void __launch_bounds__(kThreads, ZO_PASS1_MIN_CTAS) pass1_kernel(cons
           }
         }
       }
-      acc.add(x);
+      if (NB == 1) acc.add<true>(x);
+      else acc.add<false>(x);
     }
   }
 
@@ -410,20 +433,6 @@ __device__ __forceinline__ void adam_elem(float sj, float& p, float& m, float& v
   const float den = __fadd_rn(__fmul_rn(__fsqrt_rn(v), c.isb2), c.eps);
   p = __fmul_rn(p, c.decay);
   p = __fsub_rn(p, __fmul_rn(c.step_size, __fdiv_rn(m, den)));
-}
-
-// The same sequence on two elements at once with packed fp32x2 arithmetic
-// (identical rounding per lane); square root and division stay scalar.
-__device__ __forceinline__ void adam_pair(float2 s, float2& p, float2& m, float2& v,
-                                          const Scalars& c) {
-  const float2 g = mul2(s, make_float2(c.coef, c.coef));
-  m = add2(mul2(make_float2(c.b1, c.b1), m), mul2(make_float2(c.omb1, c.omb1), g));
-  v = add2(mul2(make_float2(c.b2, c.b2), v), mul2(make_float2(c.omb2, c.omb2), mul2(g, g)));
-  const float2 r = make_float2(__fsqrt_rn(v.x), __fsqrt_rn(v.y));
-  const float2 den = add2(mul2(r, make_float2(c.isb2, c.isb2)), make_float2(c.eps, c.eps));
-  p = mul2(p, make_float2(c.decay, c.decay));
-  const float2 q = make_float2(__fdiv_rn(m.x, den.x), __fdiv_rn(m.y, den.y));
-  p = sub2(p, mul2(make_float2(c.step_size, c.step_size), q));
 }
 
 __device__ __forceinline__ void f4_to(const float4& a, float* d) {
@@ -496,18 +505,7 @@ __global__ void __launch_bounds__(kThreads, ZO_PASS2_MIN_CTAS) pass2_kernel(cons
       f4_to(__ldcs(vm), v);
       f4_to(__ldcs(vm + 1), v + 4);
 #pragma unroll
-      for (int i = 0; i < kVec / 2; ++i) {
-        float2 pp = make_float2(p[2 * i], p[2 * i + 1]);
-        float2 mm2 = make_float2(m[2 * i], m[2 * i + 1]);
-        float2 vv = make_float2(v[2 * i], v[2 * i + 1]);
-        adam_pair(make_float2(x[2 * i], x[2 * i + 1]), pp, mm2, vv, c);
-        p[2 * i] = pp.x;
-        p[2 * i + 1] = pp.y;
-        m[2 * i] = mm2.x;
-        m[2 * i + 1] = mm2.y;
-        v[2 * i] = vv.x;
-        v[2 * i + 1] = vv.y;
-      }
+      for (int i = 0; i < kVec; ++i) adam_elem(x[i], p[i], m[i], v[i], c);
       float4* po = reinterpret_cast<float4*>(s.master + e0);
       float4* mo = reinterpret_cast<float4*>(s.m + e0);
       float4* vo = reinterpret_cast<float4*>(s.v + e0);
