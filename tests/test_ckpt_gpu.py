@@ -88,8 +88,9 @@ def test_save_load_resume_is_bit_exact(tmp_path):
     steps(h3, c, c16, 5, 10)
     torch.cuda.synchronize()
     for r in range(world):
-        for x, y in zip(a[r], c[r]):
-            assert torch.equal(x.view(torch.int32), y.view(torch.int32))
+        bb, e, _, _ = O.shard_bounds(numel, world, r)
+        for x, y in zip(a[r], c[r]):       # real elements; padding is never touched
+            assert torch.equal(x[:e - bb].view(torch.int32), y[:e - bb].view(torch.int32))
         assert z.zero_opt_loss_scale(h1, r).as_tuple() == z.zero_opt_loss_scale(h3, r).as_tuple()
     assert torch.equal(a16.view(torch.int16), c16.view(torch.int16))
     z.zero_opt_destroy(h1)
