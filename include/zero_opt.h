@@ -356,6 +356,33 @@ zero_status zero_opt_load_shard(zero_opt_t h, int32_t rank, float* master, float
 zero_status zero_opt_consolidate_fp32(const char* const* paths, int32_t n_paths,
                                       int64_t numel, float* out);
 
+/* Gradient statistics for callers that cannot allocate device memory.  (No
+ * counterpart on the pages: this is a service of this library.)
+ *
+ * The same result as zero_opt_grad_stats for one shard -- the overflow flag
+ * and the sum of squares of the binary32 sums of n_bufs 16-bit gradient
+ * buffers of n elements each -- but with no handle and no allocation.  Some
+ * callers may not call cudaMalloc: a runtime whose own allocator owns every
+ * device byte, a process already at its memory limit, or a code path that
+ * cannot afford the device-wide synchronization cudaMalloc may cause; a
+ * handle (zero_opt_create) allocates a workspace, so those callers use this.
+ *
+ * grads: host array of n_bufs device pointers (fp16 or bf16 per grad_dtype),
+ * summed in index order; n_bufs must be 1..64 (ERANGE beyond 64).  out: a
+ * DEVICE pointer to one zero_opt_stats, written asynchronously on `stream`.
+ * Its scratch is a fixed 12,544-byte array in the library's device image
+ * (per-CTA partial sums for at most 1024 CTAs and a completion counter),
+ * held by every GPU that loads the library until the process exits.  The
+ * first call on a device looks up that array's device address (with that
+ * device current); make that first call before any stream capture.  Every
+ * call shares the array, so calls that may overlap on the GPU (different
+ * streams, or different host threads) race and must be serialized by the
+ * caller.  Errors: EINVAL (NULL grads/out, a NULL gradient pointer with
+ * n > 0, n < 0, n_bufs < 1, bad dtype), ERANGE (n_bufs > 64), ECUDA. */
+zero_status zero_opt_grad_stats_noalloc(const void* const* grads, int32_t n_bufs,
+                                        int32_t grad_dtype, int64_t n, void* stream,
+                                        zero_opt_stats* out);
+
 /* Static string describing a status code; never NULL. */
 const char* zero_opt_status_string(zero_status s);
 

@@ -114,6 +114,7 @@ SIGNATURES = [
     ("zero_opt_save_shard", _i32, [_vp, _i32, _vp, _vp, _vp, _vp, ctypes.c_char_p]),
     ("zero_opt_load_shard", _i32, [_vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp, ctypes.c_char_p]),
     ("zero_opt_consolidate_fp32", _i32, [_P(ctypes.c_char_p), _i32, _i64, _vp]),
+    ("zero_opt_grad_stats_noalloc", _i32, [_P(_vp), _i32, _i32, _i64, _vp, _vp]),
     ("zero_opt_status_string", ctypes.c_char_p, [_i32]),
     ("zero_opt_last_error", ctypes.c_char_p, []),
 ]
@@ -429,3 +430,14 @@ def zero_opt_consolidate_fp32(paths, numel: int):
     _check(lib().zero_opt_consolidate_fp32(arr, len(paths), numel, _np_ptr(out)),
            "zero_opt_consolidate_fp32")
     return out
+
+
+def zero_opt_grad_stats_noalloc(grads, grad_dtype: int, n: int, out, stream=None) -> None:
+    """Statistics of the sum of `grads` (device tensors) written into `out`, a
+    device buffer of at least 16 bytes holding one zero_opt_stats; allocates
+    nothing on the device."""
+    grads = list(grads)
+    arr = _ptr_array(grads)
+    _check(lib().zero_opt_grad_stats_noalloc(ctypes.cast(arr, _P(_vp)), len(grads), grad_dtype,
+                                             n, _stream(stream), _ptr(out)),
+           "zero_opt_grad_stats_noalloc")

@@ -10,7 +10,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 INCLUDE = os.path.join(ROOT, "include")
 CSRC = os.path.join(PKG, "csrc")
-SOURCES = [os.path.join(CSRC, "zero_opt.cu"), os.path.join(CSRC, "ckpt.cpp")]
+SOURCES = [os.path.join(CSRC, "zero_opt.cu"), os.path.join(CSRC, "ckpt.cpp"),
+           os.path.join(CSRC, "noalloc.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("kernels.cuh", "zero_opt_internal.h",
                                                      "host_util.h")] + [
     os.path.join(INCLUDE, "zero_opt.h")]
@@ -53,7 +54,8 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
             print(r.stdout + r.stderr)
         os.replace(tmp, LIB)
     except subprocess.CalledProcessError as e:
-        os.unlink(tmp)
+        if os.path.exists(tmp):
+            os.unlink(tmp)
         raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + e.stderr) from e
     return LIB
 

@@ -232,7 +232,7 @@ __device__ __forceinline__ double block_sum(double x, double* red) {
 // clip coefficient min(1, max_norm / (norm + 1e-6)), Adam step t += 1 with its
 // bias corrections, and the scale grows by the factor after `window`
 // consecutive applied steps.
-__device__ void decide(const Pass1Args& a, double own_sumsq, int own_flag) {
+static __device__ void decide(const Pass1Args& a, double own_sumsq, int own_flag) {
   Workspace* ws = a.ws;
   ws->ticket = 0u;
   if (a.mode == kStatsOnly) {
