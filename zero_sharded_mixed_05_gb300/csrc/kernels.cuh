@@ -1,8 +1,9 @@
 // kernels.cuh -- sm_103a kernels of the per-shard mixed-precision ZeRO step.
 //
-// pass1_kernel (steps a1..a4): each CTA walks its tiles of the shard, sums the
-//   R*K 16-bit gradient buffers per element in binary32 (rank-major order,
-//   starting from +0), optionally stores the sums (the stash), and accumulates
+// pass1_single_kernel / pass1_multi_kernel (steps a1..a4): each CTA walks its
+//   tiles of the shard, sums the R*K 16-bit gradient buffers per element in
+//   binary32 (rank-major order, starting from +0; one buffer or many),
+//   optionally stores the sums (the stash), and accumulates
 //   the overflow flag and the sum of squares.  CTAs publish one partial each;
 //   the CTA that finishes last (atomic ticket, no waiting) folds the partials
 //   in CTA order in binary64, takes the per-step decisions (skip, clip
@@ -45,6 +46,11 @@
 #ifndef ZO_PASS1_UNROLL
 #define ZO_PASS1_UNROLL 4
 #endif
+// 1: the single-buffer sum of squares runs both TwoSum lanes as packed
+// FADD2/FMUL2 instructions.
+#ifndef ZO_PACKED_TWOSUM
+#define ZO_PACKED_TWOSUM 0
+#endif
 
 namespace zo {
 
@@ -69,6 +75,14 @@ struct Fmt<__half> {
       f[2 * i + 1] = t.y;
     }
   }
+  // the two fp16 values of a 32-bit word, low half first
+  static __device__ __forceinline__ float2 dec2(uint32_t w) {
+    return __half22float2(*reinterpret_cast<const __half2*>(&w));
+  }
+  static constexpr uint32_t kInf = 0x7C00u;      // |bits| >= kInf: inf or NaN
+  // Every finite fp16 value lies in [2^-24, 2^16): inside the exact range of
+  // the sum of squares, so only inf/NaN leave the fast path.
+  static __device__ __forceinline__ bool fast16(uint32_t t16) { return t16 < kInf; }
   static __device__ __forceinline__ uint4 enc8(const float (&f)[kVec]) {
     uint4 u;
     __half2* h = reinterpret_cast<__half2*>(&u);
@@ -94,6 +108,15 @@ struct Fmt<__nv_bfloat16> {
       f[2 * i] = t.x;
       f[2 * i + 1] = t.y;
     }
+  }
+  // bf16 is the upper half of binary32: the widening is a shift or a mask
+  static __device__ __forceinline__ float2 dec2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+  }
+  static constexpr uint32_t kInf = 0x7F80u;
+  // fast range [2^-40, 2^50) (or all zero), as for binary32 sums
+  static __device__ __forceinline__ bool fast16(uint32_t t16) {
+    return t16 < 0x5880u && (t16 >= 0x2B80u || t16 == 0u);
   }
   static __device__ __forceinline__ uint4 enc8(const float (&f)[kVec]) {
     uint4 u;
@@ -126,8 +149,37 @@ struct RunCursor {
   }
 };
 
+// The fields of a run that pass 1 needs (it never touches master/m/v/p16),
+// so that the cursor costs few registers.
+struct RunCursorLite {
+  int64_t begin = 0, end = 0;
+  struct {
+    int64_t tile0, n, stash_off;
+    int32_t gbase, vec;
+  } s;
+  __device__ __forceinline__ void seek(const Seg* __restrict__ segs, int nseg,
+                                       int64_t tile) {
+    if (tile >= begin && tile < end) return;
+    int lo = 0, hi = nseg - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (segs[mid].tile0 <= tile) lo = mid;
+      else hi = mid - 1;
+    }
+    const Seg& g = segs[lo];
+    s.tile0 = g.tile0;
+    s.n = g.n;
+    s.stash_off = g.stash_off;
+    s.gbase = g.gbase;
+    s.vec = g.vec;
+    begin = g.tile0;
+    end = g.tile0 + g.ntiles;
+  }
+};
+
+template <typename S>
 __device__ __forceinline__ const unsigned short* grad_ptr(const void* const* gptrs,
-                                                          const Seg& s, int b) {
+                                                          const S& s, int b) {
   const unsigned long long raw =
       __ldg(reinterpret_cast<const unsigned long long*>(gptrs) + s.gbase + b);
   return reinterpret_cast<const unsigned short*>(raw);
@@ -202,6 +254,63 @@ struct SqAcc {
       slow = __dadd_rn(slow, d);
     }
   }
+  // Eight raw 16-bit gradients of a single buffer (the sum is the value
+  // itself).  The range and overflow checks run on the 16-bit patterns, two
+  // at a time (__vmaxu2); the squares are exact in binary32.
+  uint32_t amax16 = 0u;
+  template <typename GT>
+  __device__ __forceinline__ void add_raw16(const uint4& r) {
+    const uint32_t m01 = __vmaxu2(r.x & 0x7fff7fffu, r.y & 0x7fff7fffu);
+    const uint32_t m23 = __vmaxu2(r.z & 0x7fff7fffu, r.w & 0x7fff7fffu);
+    const uint32_t mm = __vmaxu2(m01, m23);
+    const uint32_t t16 = max(mm & 0xffffu, mm >> 16);
+    amax16 = max(amax16, t16);
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+    if (Fmt<GT>::fast16(t16)) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 x = Fmt<GT>::dec2(w[k]);
+#if ZO_PACKED_TWOSUM
+        two_sum_add_exact2(x);
+#else
+        two_sum_add_exact(hi0, lo0, x.x);
+        two_sum_add_exact(hi1, lo1, x.y);
+#endif
+      }
+    } else {
+      double d = 0.0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 x = Fmt<GT>::dec2(w[k]);
+        d = __dadd_rn(d, __dmul_rn((double)x.x, (double)x.x));
+        d = __dadd_rn(d, __dmul_rn((double)x.y, (double)x.y));
+      }
+      slow = __dadd_rn(slow, d);
+    }
+  }
+#if ZO_PACKED_TWOSUM
+  // Both lanes of TwoSum with packed binary32 instructions (each lane rounds
+  // like the scalar _rn operation).
+  __device__ __forceinline__ void two_sum_add_exact2(float2 x) {
+    float2 hi = make_float2(hi0, hi1), lo = make_float2(lo0, lo1);
+    const float2 p = __fmul2_rn(x, x);
+    const float2 t = __fadd2_rn(hi, p);
+    const float2 bp = __fadd2_rn(t, make_float2(-hi.x, -hi.y));
+    const float2 ap = __fadd2_rn(t, make_float2(-bp.x, -bp.y));
+    const float2 d1 = __fadd2_rn(hi, make_float2(-ap.x, -ap.y));
+    const float2 d2 = __fadd2_rn(p, make_float2(-bp.x, -bp.y));
+    lo = __fadd2_rn(lo, __fadd2_rn(d1, d2));
+    hi0 = t.x;
+    hi1 = t.y;
+    lo0 = lo.x;
+    lo1 = lo.y;
+  }
+#endif
+  template <typename GT>
+  __device__ __forceinline__ bool overflowed() const {
+    return amax >= 0x7f800000u || amax16 >= Fmt<GT>::kInf;
+  }
+
   __device__ __forceinline__ double total() const {
     const double a = __dadd_rn((double)hi0, (double)lo0);
     const double b = __dadd_rn((double)hi1, (double)lo1);
@@ -299,103 +408,12 @@ static __device__ void decide(const Pass1Args& a, double own_sumsq, int own_flag
 }
 
 // ------------------------------------------------------------- pass 1
-// NB == 1: exactly one gradient buffer; four tiles are loaded before any is
-// reduced so that each thread keeps four 16-byte loads in flight.
-// NB == 0: any number of buffers, loaded in batches of eight per tile.
-template <typename GT, bool STASH, int NB>
-__global__ void __launch_bounds__(kThreads, ZO_PASS1_MIN_CTAS) pass1_kernel(const Pass1Args a) {
-  __shared__ double red[kThreads / 32];
-  __shared__ int s_last;
-  constexpr int U = (NB == 1) ? ZO_PASS1_UNROLL : 1;
+// The epilogue shared by both pass-1 kernels: one binary64 partial and one
+// overflow flag per CTA; the CTA that finishes last folds them in CTA order
+// and takes the decisions.
+__device__ __forceinline__ void pass1_finish(const Pass1Args& a, double mine, int flag,
+                                             double* red, int* s_last) {
   const int tid = threadIdx.x;
-  const int64_t G = gridDim.x;
-  SqAcc acc;
-  RunCursor cur;
-
-  for (int64_t t0 = blockIdx.x; t0 < a.ntiles; t0 += U * G) {
-    uint4 raw[U];
-    bool fast[U];
-    if (NB == 1) {
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int64_t tile = t0 + u * G;
-        fast[u] = false;
-        if (tile < a.ntiles) {
-          cur.seek(a.segs, a.nseg, tile);
-          const int64_t e0 = (tile - cur.s.tile0) * kTile + tid * kVec;
-          if (cur.s.vec && e0 + kVec <= cur.s.n) {
-            raw[u] = __ldcg(reinterpret_cast<const uint4*>(grad_ptr(a.gptrs, cur.s, 0) + e0));
-            fast[u] = true;
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t tile = t0 + u * G;
-      if (tile >= a.ntiles) continue;
-      cur.seek(a.segs, a.nseg, tile);
-      const Seg& s = cur.s;
-      const int64_t base = (tile - s.tile0) * kTile;
-      const int64_t e0 = base + tid * kVec;
-      const bool vec = s.vec && e0 + kVec <= s.n;
-      float x[kVec];
-      if (NB == 1 && fast[u]) {
-        // one buffer: the sum is 0 + g, which differs from g only in the sign
-        // of a zero -- irrelevant to the statistics and never stored here
-        // (a single buffer is never stashed)
-        Fmt<GT>::dec8(raw[u], x);
-      } else if (NB != 1 && vec) {
-#pragma unroll
-        for (int i = 0; i < kVec; ++i) x[i] = 0.0f;
-        for (int b0 = 0; b0 < a.nbuf; b0 += 8) {
-          uint4 r[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if (b0 + j < a.nbuf)
-              r[j] = __ldcg(reinterpret_cast<const uint4*>(grad_ptr(a.gptrs, s, b0 + j) + e0));
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            if (b0 + j < a.nbuf) {
-              float y[kVec];
-              Fmt<GT>::dec8(r[j], y);
-#pragma unroll
-              for (int i = 0; i < kVec; ++i) x[i] = __fadd_rn(x[i], y[i]);
-            }
-          }
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < kVec; ++i) {
-          const int64_t e = s.vec ? e0 + i : base + (int64_t)i * kThreads + tid;
-          float sum = 0.0f;
-          if (e < s.n) {
-            for (int b = 0; b < a.nbuf; ++b)
-              sum = __fadd_rn(sum, Fmt<GT>::dec(__ldcg(grad_ptr(a.gptrs, s, b) + e)));
-          }
-          x[i] = sum;
-        }
-      }
-      if (STASH) {
-        float* dst = a.stash + s.stash_off;
-        if (vec) {
-          reinterpret_cast<float4*>(dst + e0)[0] = make_float4(x[0], x[1], x[2], x[3]);
-          reinterpret_cast<float4*>(dst + e0)[1] = make_float4(x[4], x[5], x[6], x[7]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < kVec; ++i) {
-            const int64_t e = s.vec ? e0 + i : base + (int64_t)i * kThreads + tid;
-            if (e < s.n) dst[e] = x[i];
-          }
-        }
-      }
-      if (NB == 1) acc.add<true>(x);
-      else acc.add<false>(x);
-    }
-  }
-
-  const double mine = acc.total();
-  const int flag = acc.amax >= 0x7f800000u ? 1 : 0;
   const double blk = block_sum(mine, red);
   const int any = __syncthreads_or(flag);
   if (tid == 0) {
@@ -403,10 +421,10 @@ __global__ void __launch_bounds__(kThreads, ZO_PASS1_MIN_CTAS) pass1_kernel(cons
     a.ws->part_flag[blockIdx.x] = any;
     __threadfence();
     const unsigned int prev = atomicAdd(&a.ws->ticket, 1u);
-    s_last = (prev == gridDim.x - 1) ? 1 : 0;
+    *s_last = (prev == gridDim.x - 1) ? 1 : 0;
   }
   __syncthreads();
-  if (!s_last) return;
+  if (!*s_last) return;
   __threadfence();
   double part = 0.0;
   int f = 0;
@@ -417,6 +435,129 @@ __global__ void __launch_bounds__(kThreads, ZO_PASS1_MIN_CTAS) pass1_kernel(cons
   const double tot = block_sum(part, red);
   const int anyf = __syncthreads_or(f);
   if (tid == 0) decide(a, tot, anyf);
+}
+
+// One tile element by element: a ragged tail of a vector run (e >= e0 within
+// the thread's 8 elements) or any tile of a run with a misaligned pointer
+// (elements base + i*256 + tid, coalesced).  Kept out of line: it is rare, and
+// inlining it would cost the main loops registers.
+template <typename GT, bool STASH>
+__device__ __noinline__ void pass1_elementwise_tile(const Pass1Args& a, int64_t n,
+                                                    int64_t stash_off, int32_t gbase,
+                                                    int32_t vec, int64_t base, SqAcc& acc) {
+  const int tid = threadIdx.x;
+  const int64_t e0 = base + tid * kVec;
+  float x[kVec];
+#pragma unroll
+  for (int i = 0; i < kVec; ++i) {
+    const int64_t e = vec ? e0 + i : base + (int64_t)i * kThreads + tid;
+    float sum = 0.0f;
+    if (e < n) {
+      for (int b = 0; b < a.nbuf; ++b) {
+        const unsigned long long raw =
+            __ldg(reinterpret_cast<const unsigned long long*>(a.gptrs) + gbase + b);
+        sum = __fadd_rn(sum, Fmt<GT>::dec(__ldcg(reinterpret_cast<const unsigned short*>(raw) + e)));
+      }
+      if (STASH) a.stash[stash_off + e] = sum;
+    }
+    x[i] = sum;
+  }
+  acc.add<false>(x);
+}
+
+// Single gradient buffer (R*K = 1, never stashed).  ZO_PASS1_UNROLL tiles'
+// 16-byte loads are issued before any is reduced; reduction works on the raw
+// 16-bit words (SqAcc::add_raw16).
+template <typename GT>
+__global__ void __launch_bounds__(kThreads, ZO_PASS1_MIN_CTAS)
+    pass1_single_kernel(const Pass1Args a) {
+  __shared__ double red[kThreads / 32];
+  __shared__ int s_last;
+  constexpr int U = ZO_PASS1_UNROLL;
+  const int tid = threadIdx.x;
+  const int64_t G = gridDim.x;
+  SqAcc acc;
+  RunCursorLite cur;
+  for (int64_t t0 = blockIdx.x; t0 < a.ntiles; t0 += U * G) {
+    uint4 raw[U];
+    bool fast[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t tile = t0 + u * G;
+      fast[u] = false;
+      if (tile < a.ntiles) {
+        cur.seek(a.segs, a.nseg, tile);
+        const int64_t e0 = (tile - cur.s.tile0) * kTile + tid * kVec;
+        if (cur.s.vec && e0 + kVec <= cur.s.n) {
+          raw[u] = __ldcg(reinterpret_cast<const uint4*>(grad_ptr(a.gptrs, cur.s, 0) + e0));
+          fast[u] = true;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t tile = t0 + u * G;
+      if (tile >= a.ntiles) continue;
+      if (fast[u]) {
+        // the sum is 0 + g, which differs from g only in the sign of a zero
+        // (irrelevant to the statistics)
+        acc.add_raw16<GT>(raw[u]);
+      } else {
+        cur.seek(a.segs, a.nseg, tile);
+        pass1_elementwise_tile<GT, false>(a, cur.s.n, cur.s.stash_off, cur.s.gbase, cur.s.vec,
+                                          (tile - cur.s.tile0) * kTile, acc);
+      }
+    }
+  }
+  pass1_finish(a, acc.total(), acc.overflowed<GT>() ? 1 : 0, red, &s_last);
+}
+
+// Any number of gradient buffers, loaded in batches of eight per tile, summed
+// in buffer order; optionally stores the sums (the stash).
+template <typename GT, bool STASH>
+__global__ void __launch_bounds__(kThreads, ZO_PASS1_MIN_CTAS)
+    pass1_multi_kernel(const Pass1Args a) {
+  __shared__ double red[kThreads / 32];
+  __shared__ int s_last;
+  const int tid = threadIdx.x;
+  SqAcc acc;
+  RunCursorLite cur;
+  for (int64_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
+    cur.seek(a.segs, a.nseg, tile);
+    const auto& s = cur.s;
+    const int64_t base = (tile - s.tile0) * kTile;
+    const int64_t e0 = base + tid * kVec;
+    if (!(s.vec && e0 + kVec <= s.n)) {
+      pass1_elementwise_tile<GT, STASH>(a, s.n, s.stash_off, s.gbase, s.vec, base, acc);
+      continue;
+    }
+    float x[kVec];
+#pragma unroll
+    for (int i = 0; i < kVec; ++i) x[i] = 0.0f;
+    for (int b0 = 0; b0 < a.nbuf; b0 += 8) {
+      uint4 r[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (b0 + j < a.nbuf)
+          r[j] = __ldcg(reinterpret_cast<const uint4*>(grad_ptr(a.gptrs, s, b0 + j) + e0));
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (b0 + j < a.nbuf) {
+          float y[kVec];
+          Fmt<GT>::dec8(r[j], y);
+#pragma unroll
+          for (int i = 0; i < kVec; ++i) x[i] = __fadd_rn(x[i], y[i]);
+        }
+      }
+    }
+    if (STASH) {
+      float* dst = a.stash + s.stash_off + e0;
+      reinterpret_cast<float4*>(dst)[0] = make_float4(x[0], x[1], x[2], x[3]);
+      reinterpret_cast<float4*>(dst)[1] = make_float4(x[4], x[5], x[6], x[7]);
+    }
+    acc.add<false>(x);
+  }
+  pass1_finish(a, acc.total(), acc.overflowed<GT>() ? 1 : 0, red, &s_last);
 }
 
 // ------------------------------------------------------------- pass 2

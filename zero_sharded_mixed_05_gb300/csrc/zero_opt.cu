@@ -257,15 +257,14 @@ using Pass1Fn = void (*)(zo::Pass1Args);
 using Pass2Fn = void (*)(zo::Pass2Args);
 
 Pass1Fn pick_pass1(int gdt, bool stash, bool one) {
+  // a single buffer is never stashed (the stash needs more than four)
   if (gdt == ZERO_FP16) {
-    if (stash) return one ? zo::pass1_kernel<__half, true, 1> : zo::pass1_kernel<__half, true, 0>;
-    return one ? zo::pass1_kernel<__half, false, 1> : zo::pass1_kernel<__half, false, 0>;
+    if (one) return zo::pass1_single_kernel<__half>;
+    return stash ? zo::pass1_multi_kernel<__half, true> : zo::pass1_multi_kernel<__half, false>;
   }
-  if (stash)
-    return one ? zo::pass1_kernel<__nv_bfloat16, true, 1>
-               : zo::pass1_kernel<__nv_bfloat16, true, 0>;
-  return one ? zo::pass1_kernel<__nv_bfloat16, false, 1>
-             : zo::pass1_kernel<__nv_bfloat16, false, 0>;
+  if (one) return zo::pass1_single_kernel<__nv_bfloat16>;
+  return stash ? zo::pass1_multi_kernel<__nv_bfloat16, true>
+               : zo::pass1_multi_kernel<__nv_bfloat16, false>;
 }
 
 template <typename GT, typename PT>
