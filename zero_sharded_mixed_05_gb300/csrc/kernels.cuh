@@ -46,11 +46,6 @@
 #ifndef ZO_PASS1_UNROLL
 #define ZO_PASS1_UNROLL 4
 #endif
-// 1: the single-buffer sum of squares runs both TwoSum lanes as packed
-// FADD2/FMUL2 instructions.
-#ifndef ZO_PACKED_TWOSUM
-#define ZO_PACKED_TWOSUM 0
-#endif
 
 namespace zo {
 
@@ -270,12 +265,8 @@ struct SqAcc {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const float2 x = Fmt<GT>::dec2(w[k]);
-#if ZO_PACKED_TWOSUM
-        two_sum_add_exact2(x);
-#else
         two_sum_add_exact(hi0, lo0, x.x);
         two_sum_add_exact(hi1, lo1, x.y);
-#endif
       }
     } else {
       double d = 0.0;
@@ -288,24 +279,6 @@ struct SqAcc {
       slow = __dadd_rn(slow, d);
     }
   }
-#if ZO_PACKED_TWOSUM
-  // Both lanes of TwoSum with packed binary32 instructions (each lane rounds
-  // like the scalar _rn operation).
-  __device__ __forceinline__ void two_sum_add_exact2(float2 x) {
-    float2 hi = make_float2(hi0, hi1), lo = make_float2(lo0, lo1);
-    const float2 p = __fmul2_rn(x, x);
-    const float2 t = __fadd2_rn(hi, p);
-    const float2 bp = __fadd2_rn(t, make_float2(-hi.x, -hi.y));
-    const float2 ap = __fadd2_rn(t, make_float2(-bp.x, -bp.y));
-    const float2 d1 = __fadd2_rn(hi, make_float2(-ap.x, -ap.y));
-    const float2 d2 = __fadd2_rn(p, make_float2(-bp.x, -bp.y));
-    lo = __fadd2_rn(lo, __fadd2_rn(d1, d2));
-    hi0 = t.x;
-    hi1 = t.y;
-    lo0 = lo.x;
-    lo1 = lo.y;
-  }
-#endif
   template <typename GT>
   __device__ __forceinline__ bool overflowed() const {
     return amax >= 0x7f800000u || amax16 >= Fmt<GT>::kInf;
