@@ -159,9 +159,14 @@ typedef struct zero_opt_step_info {
   double norm;              /* L2 norm of the unscaled gradient (NaN on skip) */
   float coef;               /* factor applied to each reduced sum            */
   float scale_used;         /* loss scale the gradients carried              */
-  int32_t skipped;          /* 1 if the step was skipped (overflow)          */
+  int32_t skipped;          /* 1 if the step was skipped (overflow or fault) */
   int32_t nonfinite;
   int64_t t;                /* Adam step counter after the step              */
+  int32_t fault;            /* 1 if a kernel gave up waiting for its own data
+                               copies (bounded wait expired): the step was
+                               skipped and nothing, the loss scale included,
+                               was changed                                   */
+  int32_t reserved;
 } zero_opt_step_info;
 
 /* Loss-scaler state of one rank. */
@@ -289,6 +294,16 @@ zero_status zero_opt_last_step(zero_opt_t h, void* stream, zero_opt_step_info* o
  * the stream it runs on.  Host only; records nothing by itself.
  * Errors: EINVAL (h NULL). */
 zero_status zero_opt_set_events(zero_opt_t h, void* ev_start, void* ev_mid, void* ev_end);
+
+/* Failure-detection test hook.  The next statistics pass of this handle that
+ * stages a single gradient buffer through shared memory leaves one of its
+ * copy barriers un-armed, so that the wait for it expires after its bound
+ * (about a second).  The kernel then stops, waits (bounded) for its copies in
+ * flight, and records a fault: that step is skipped without changing any
+ * state, and zero_opt_last_step reports fault = 1.  Nothing hangs and the
+ * context stays usable.  Host only; the hook arms one launch.
+ * Errors: EINVAL (h NULL). */
+zero_status zero_opt_inject_wait_fault(zero_opt_t h);
 
 /* Kernels launched by this handle since creation (for launch accounting). */
 zero_status zero_opt_launch_count(zero_opt_t h, int64_t* launches);

@@ -60,7 +60,8 @@ class zero_opt_stats(ctypes.Structure):
 
 class zero_opt_step_info(ctypes.Structure):
     _fields_ = [("sumsq", _f64), ("norm", _f64), ("coef", _f32), ("scale_used", _f32),
-                ("skipped", _i32), ("nonfinite", _i32), ("t", _i64)]
+                ("skipped", _i32), ("nonfinite", _i32), ("t", _i64), ("fault", _i32),
+                ("reserved", _i32)]
 
 
 class zero_opt_scaler_state(ctypes.Structure):
@@ -108,6 +109,7 @@ SIGNATURES = [
     ("zero_opt_set_lr", _i32, [_vp, _f64]),
     ("zero_opt_last_step", _i32, [_vp, _vp, _P(zero_opt_step_info)]),
     ("zero_opt_set_events", _i32, [_vp, _vp, _vp, _vp]),
+    ("zero_opt_inject_wait_fault", _i32, [_vp]),
     ("zero_opt_launch_count", _i32, [_vp, _P(_i64)]),
     ("zero_opt_ckpt_write", _i32, [ctypes.c_char_p, _P(zero_opt_ckpt_info), _vp, _vp, _vp]),
     ("zero_opt_ckpt_read", _i32, [ctypes.c_char_p, _P(zero_opt_ckpt_info), _vp, _vp, _vp]),
@@ -342,6 +344,11 @@ def zero_opt_set_events(h, ev_start=None, ev_mid=None, ev_end=None) -> None:
         return e.cuda_event
     _check(lib().zero_opt_set_events(h, raw(ev_start), raw(ev_mid), raw(ev_end)),
            "zero_opt_set_events")
+
+
+def zero_opt_inject_wait_fault(h) -> None:
+    """Arm the failure-detection test hook for the next statistics pass."""
+    _check(lib().zero_opt_inject_wait_fault(h), "zero_opt_inject_wait_fault")
 
 
 def zero_opt_launch_count(h) -> int:

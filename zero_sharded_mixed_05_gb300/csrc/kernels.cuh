@@ -317,15 +317,36 @@ __device__ __forceinline__ double block_sum(double x, double* red) {
 static __device__ void decide(const Pass1Args& a, double own_sumsq, int own_flag) {
   Workspace* ws = a.ws;
   ws->ticket = 0u;
+  const int fault = ws->fault;
+  ws->fault = 0;
   if (a.mode == kStatsOnly) {
-    ws->own_sumsq = own_sumsq;
-    ws->own_nonfinite = own_flag;
+    // after a fault the statistics are incomplete: report an overflow so that
+    // every rank that folds them skips the step
+    ws->own_sumsq = fault ? __longlong_as_double(0x7ff8000000000000ll) : own_sumsq;
+    ws->own_nonfinite = fault ? 1 : own_flag;
+    return;
+  }
+  if (fault) {
+    // a bounded wait expired: skip without touching the scaler state
+    Decision d;
+    d.sumsq = d.norm = __longlong_as_double(0x7ff8000000000000ll);
+    d.coef = d.scale_used = 0.0f;
+    d.skip = 1;
+    d.nonfinite = 0;
+    d.t = a.ranks[a.rank].t;
+    d.fault = 1;
+    d.pad_ = 0;
+    d.step_size = d.isb2 = d.decay = d.b1 = d.omb1 = d.b2 = d.omb2 = d.eps = 0.0f;
+    d.scale_used = a.ranks[a.rank].scale;
+    ws->dec = d;
     return;
   }
   const double sumsq = a.mode == kStepGlobal ? a.g_sumsq : own_sumsq;
   const int nonfinite = a.mode == kStepGlobal ? a.g_nonfinite : own_flag;
   RankState st = a.ranks[a.rank];
   Decision d;
+  d.fault = 0;
+  d.pad_ = 0;
   d.sumsq = sumsq;
   d.nonfinite = nonfinite;
   d.scale_used = st.scale;
@@ -480,6 +501,145 @@ __global__ void __launch_bounds__(kThreads, ZO_PASS1_MIN_CTAS)
         pass1_elementwise_tile<GT, false>(a, cur.s.n, cur.s.stash_off, cur.s.gbase, cur.s.vec,
                                           (tile - cur.s.tile0) * kTile, acc);
       }
+    }
+  }
+  pass1_finish(a, acc.total(), acc.overflowed<GT>() ? 1 : 0, red, &s_last);
+}
+
+// ------------------------------------------------------------- bulk copies
+// Thin wrappers of the PTX for Blackwell's asynchronous bulk copies (TMA) and
+// shared-memory transaction barriers.
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(unsigned long long* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// Arrive (the one expected arrival) and expect `bytes` of asynchronous copies.
+__device__ __forceinline__ void mbar_arrive_expect_tx(unsigned long long* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(unsigned long long* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+// Global -> shared copy of `bytes` (multiple of 16, both addresses 16-byte
+// aligned) that completes its bytes on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          unsigned long long* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait for the phase of `bar` with the given parity, giving up after about a
+// second (returns false then).  No wait in this library is unbounded.
+__device__ __forceinline__ bool mbar_wait_bounded(unsigned long long* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > 1000000000ull) return false;
+  }
+  return true;
+}
+
+#ifndef ZO_BULK_STAGES
+#define ZO_BULK_STAGES 8
+#endif
+
+// Single gradient buffer, staged through shared memory by bulk copies: thread
+// 0 keeps ZO_BULK_STAGES tiles (4 KiB each for 16-bit gradients) in flight per
+// CTA, so the reducing threads never wait on global memory.  A tile that is
+// not a full 16-byte aligned tile (a run's ragged tail, a misaligned run) is
+// not copied: its barrier phase is completed by a plain arrival and the tile
+// is reduced element by element from global memory.  If a wait expires the
+// CTA stops issuing copies, waits (again bounded) for those in flight, and
+// records a fault, which makes the step a no-op.
+template <typename GT>
+__global__ void __launch_bounds__(kThreads, ZO_PASS1_MIN_CTAS)
+    pass1_bulk_kernel(const Pass1Args a) {
+  constexpr int S = ZO_BULK_STAGES;
+  __shared__ __align__(128) uint4 buf[S][kThreads];
+  __shared__ __align__(8) unsigned long long bar[S];
+  __shared__ double red[kThreads / 32];
+  __shared__ int s_last, s_err;
+  const int tid = threadIdx.x;
+  const int64_t G = gridDim.x;
+  const int64_t mine = (a.ntiles > (int64_t)blockIdx.x)
+                           ? (a.ntiles - 1 - (int64_t)blockIdx.x) / G + 1
+                           : 0;
+  RunCursorLite pcur;  // thread 0's cursor for issuing copies
+  auto issue = [&](int64_t i) {
+    const int64_t tile = blockIdx.x + i * G;
+    unsigned long long* b = &bar[i % S];
+    if (a.inject_wait_fault && blockIdx.x == 0 && i == 1) return;  // test hook
+    pcur.seek(a.segs, a.nseg, tile);
+    const int64_t base = (tile - pcur.s.tile0) * kTile;
+    if (pcur.s.vec && base + kTile <= pcur.s.n) {
+      mbar_arrive_expect_tx(b, kTile * 2);
+      bulk_load(&buf[i % S][0], grad_ptr(a.gptrs, pcur.s, 0) + base, kTile * 2, b);
+    } else {
+      mbar_arrive(b);
+    }
+  };
+  if (tid == 0) {
+    for (int k = 0; k < S; ++k) mbar_init(&bar[k], 1);
+    mbar_init_fence();
+    s_err = 0;
+  }
+  __syncthreads();
+  if (tid == 0)
+    for (int64_t i = 0; i < mine && i < S; ++i) issue(i);
+  SqAcc acc;
+  RunCursorLite cur;
+  int64_t issued = mine < S ? mine : S;
+  for (int64_t i = 0; i < mine; ++i) {
+    const uint32_t parity = (uint32_t)((i / S) & 1);
+    if (!mbar_wait_bounded(&bar[i % S], parity)) s_err = 1;
+    const int64_t tile = blockIdx.x + i * G;
+    cur.seek(a.segs, a.nseg, tile);
+    const int64_t base = (tile - cur.s.tile0) * kTile;
+    if (!s_err) {
+      if (cur.s.vec && base + kTile <= cur.s.n)
+        acc.add_raw16<GT>(buf[i % S][tid]);
+      else
+        pass1_elementwise_tile<GT, false>(a, cur.s.n, cur.s.stash_off, cur.s.gbase, cur.s.vec,
+                                          base, acc);
+    }
+    __syncthreads();  // every thread is done with stage i % S
+    if (s_err) {
+      // drain the copies still in flight before the CTA's shared memory goes
+      if (tid == 0) {
+        for (int64_t j = i; j < issued; ++j)
+          (void)mbar_wait_bounded(&bar[j % S], (uint32_t)((j / S) & 1));
+        atomicExch(&a.ws->fault, 1);
+      }
+      break;
+    }
+    if (tid == 0 && issued < mine) {
+      issue(issued);
+      ++issued;
     }
   }
   pass1_finish(a, acc.total(), acc.overflowed<GT>() ? 1 : 0, red, &s_last);

@@ -23,6 +23,11 @@
 #include "kernels.cuh"
 #include "zero_opt.h"
 
+// 1: a single gradient buffer takes the bulk-copy pass 1 (pass1_bulk_kernel)
+#ifndef ZO_PASS1_BULK
+#define ZO_PASS1_BULK 1
+#endif
+
 namespace {
 thread_local std::string g_err;
 }  // namespace
@@ -97,6 +102,7 @@ struct zero_opt_handle {
   int64_t launches = 0;
   uint64_t clock = 0;
   cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};  // timing hook
+  int32_t inject_wait_fault = 0;                      // test hook, one launch
   std::vector<Plan*> plans;
   std::vector<std::pair<const void*, int>> occ;  // kernel -> CTAs per SM
   std::mutex mu;
@@ -258,6 +264,10 @@ using Pass2Fn = void (*)(zo::Pass2Args);
 
 Pass1Fn pick_pass1(int gdt, bool stash, bool one) {
   // a single buffer is never stashed (the stash needs more than four)
+#if ZO_PASS1_BULK
+  if (one) return gdt == ZERO_FP16 ? zo::pass1_bulk_kernel<__half>
+                                   : zo::pass1_bulk_kernel<__nv_bfloat16>;
+#endif
   if (gdt == ZERO_FP16) {
     if (one) return zo::pass1_single_kernel<__half>;
     return stash ? zo::pass1_multi_kernel<__half, true> : zo::pass1_multi_kernel<__half, false>;
@@ -343,6 +353,8 @@ zero_status run(zero_opt_t h, int32_t rank, const std::vector<HostRun>& runs, in
   a1.hp = hyper_of(h->cfg, divisor);
   a1.ws = h->ws;
   a1.ranks = h->ranks;
+  a1.inject_wait_fault = h->inject_wait_fault;
+  h->inject_wait_fault = 0;
 
   const void* f1 = reinterpret_cast<const void*>(
       pick_pass1(h->cfg.grad_dtype, use_stash != nullptr, nbuf == 1));
@@ -826,6 +838,12 @@ zero_status zero_opt_set_events(zero_opt_t h, void* ev_start, void* ev_mid, void
   h->ev[0] = static_cast<cudaEvent_t>(ev_start);
   h->ev[1] = static_cast<cudaEvent_t>(ev_mid);
   h->ev[2] = static_cast<cudaEvent_t>(ev_end);
+  return ZERO_OK;
+}
+
+zero_status zero_opt_inject_wait_fault(zero_opt_t h) {
+  if (!h) return fail(ZERO_EINVAL, "handle is NULL");
+  h->inject_wait_fault = 1;
   return ZERO_OK;
 }
 

@@ -50,13 +50,15 @@ struct Decision {
   int32_t skip;
   int32_t nonfinite;
   int64_t t;
+  int32_t fault;
+  int32_t pad_;
   float step_size, isb2, decay, b1, omb1, b2, omb2, eps;
 };
 static_assert(sizeof(zero_opt_step_info) <= sizeof(Decision), "layout");
 
 struct Workspace {
   unsigned int ticket;   // CTAs of pass 1 that finished; reset by the last
-  int32_t pad0;
+  int32_t fault;         // set by a CTA whose bounded wait expired; reset by decide
   Decision dec;          // written by the last CTA of pass 1, read by pass 2
   double own_sumsq;      // statistics-only result
   int32_t own_nonfinite;
@@ -88,6 +90,8 @@ struct Pass1Args {
   Hyper hp;
   Workspace* ws;
   RankState* ranks;
+  int32_t inject_wait_fault;   // test hook: leave one bulk-copy barrier un-armed
+  int32_t pad2;
 };
 
 struct Pass2Args {
