@@ -88,11 +88,15 @@ typedef struct zero_opt_config {
   double weight_decay;      /* >= 0, decoupled (AdamW): p *= 1 - lr*wd      */
   double max_grad_norm;     /* > 0 clips the global L2 norm; <= 0 disables  */
   int32_t dynamic_scale;    /* 1: dynamic loss scale; 0: fixed init_scale   */
-  int32_t hysteresis;       /* must be 1 (halve on every overflow)          */
+  int32_t hysteresis;       /* >= 1: the scale is lowered on the hysteresis-th
+                               overflow since it last changed (1: every one) */
   double init_scale;        /* > 0, e.g. 2^initial_scale_power              */
   double min_scale;         /* > 0, "min_loss_scale"                        */
   double scale_factor;      /* >= 1, 2 halves / doubles                     */
   int64_t scale_window;     /* >= 1, "loss_scale_window"                    */
+  double warmup_min_lr;     /* WarmupLR: update t uses warmup_min_lr +      */
+  double warmup_max_lr;     /*   (max - min) * min(t, T) / T, T =           */
+  int64_t warmup_num_steps; /*   warmup_num_steps; 0 keeps lr constant      */
 } zero_opt_config;
 
 /*
@@ -176,13 +180,17 @@ typedef struct zero_opt_scaler_state {
   int64_t clean_steps;      /* consecutive applied steps since last change   */
   int64_t t;                /* Adam step counter (applied updates)           */
   int64_t skipped_total;    /* skipped steps so far                          */
+  int32_t overflows;        /* overflows since the scale last changed        */
+  int32_t reserved;
 } zero_opt_scaler_state;
 
 /* Fill *cfg with the ds_config.json values of "DeepSpeed tutorial" §3.2:
  * AdamW lr 2e-5, betas (0.9, 0.999), eps 1e-8, weight_decay 0.01; dynamic
  * fp16 loss scale 2^16 (initial_scale_power 16), window 1000, min 1, factor
- * 2; bias correction on, no clipping; numel 0, world 1, fp16.  Hysteresis is
- * 1 (the page's value 2 is not supported).  Errors: EINVAL if cfg is NULL. */
+ * 2; bias correction on, no clipping; numel 0, world 1, fp16; hysteresis 2;
+ * WarmupLR off (warmup_num_steps 0; set warmup_min_lr 0, warmup_max_lr 2e-5,
+ * warmup_num_steps 1000 for the page's schedule).  Errors: EINVAL if cfg is
+ * NULL. */
 zero_status zero_opt_config_default(zero_opt_config* cfg);
 
 /* Create an optimizer handle for one data-parallel group of `world` ranks.
@@ -192,8 +200,9 @@ zero_status zero_opt_config_default(zero_opt_config* cfg);
  * calls and every launching call returns ZERO_ECUDA.
  * Errors: EINVAL (NULL pointers, numel < 0, world < 1, a dtype not in
  * zero_dtype, lr < 0, beta outside [0,1), eps <= 0, weight_decay < 0,
- * init_scale/min_scale <= 0, scale_factor < 1, scale_window < 1);
- * ENOTSUP (hysteresis != 1); ENOMEM; ECUDA.  *out is NULL on failure. */
+ * init_scale/min_scale <= 0, scale_factor < 1, scale_window < 1,
+ * hysteresis < 1, warmup_num_steps < 0, a warm-up lr < 0); ENOMEM; ECUDA.
+ * *out is NULL on failure. */
 zero_status zero_opt_create(const zero_opt_config* cfg, zero_opt_t* out);
 
 /* Destroy a handle (synchronizes the device first). NULL is accepted. */
@@ -239,10 +248,12 @@ zero_status zero_opt_fold_stats(const zero_opt_stats* per_rank, int32_t n,
  * `stream`.  `global` (host, may be NULL) is the fold of all ranks'
  * zero_opt_grad_stats for these same gradients; NULL means this shard is the
  * whole world and its own statistics decide.  On overflow the step is skipped
- * (master, m, v, param16 and t untouched) and the scale is divided by
- * scale_factor, not below min_scale; otherwise AdamW is applied and after
- * scale_window consecutive applied steps the scale is multiplied by
- * scale_factor ("DeepSpeed tutorial" §2.2, §3.2).
+ * (master, m, v, param16 and t untouched) and, on the hysteresis-th
+ * overflow since the scale last changed, the scale is divided by
+ * scale_factor, not below min_scale; otherwise AdamW is applied with the
+ * update's learning rate (lr, or the WarmupLR value) and after scale_window
+ * consecutive applied steps the scale is multiplied by scale_factor
+ * ("DeepSpeed tutorial" §2.2, §2.4, §3.2).
  * Errors: EINVAL (h/bufs/grads NULL, a NULL state or gradient pointer for a
  * non-empty shard, R or K < 1, R*K > 1024), ERANGE (rank outside [0, world)),
  * ECUDA (no device, wrong current device, or a launch failure). */
@@ -318,7 +329,8 @@ zero_status zero_opt_launch_count(zero_opt_t h, int64_t* launches);
  * uint32 reserved (0), the fields of zero_opt_ckpt_info in declaration order
  * (int64 numel, int32 world, int32 rank, int64 begin, int64 real_len, then
  * float scale, int32 last_skipped, int64 clean_steps, int64 t, int64
- * skipped_total), uint64 checksum of the payload, then the payload: real_len
+ * skipped_total, int32 overflows, int32 reserved), uint64 checksum of the
+ * payload, then the payload: real_len
  * fp32 master weights, real_len fp32 m, real_len fp32 v.  Padding is not
  * stored.  The checksum is 64-bit FNV-1a over the payload taken as 8-byte
  * little-endian words (a trailing partial word zero-extended).

@@ -63,13 +63,18 @@ class Hparams(ctypes.Structure):
                 ("dynamic_scale", ctypes.c_int32),
                 ("min_scale", ctypes.c_double),
                 ("scale_factor", ctypes.c_double),
-                ("scale_window", ctypes.c_int64)]
+                ("scale_window", ctypes.c_int64),
+                ("hysteresis", ctypes.c_int64),
+                ("warmup_min_lr", ctypes.c_double),
+                ("warmup_max_lr", ctypes.c_double),
+                ("warmup_num_steps", ctypes.c_int64)]
 
 
 class Scaler(ctypes.Structure):
     _fields_ = [("scale", ctypes.c_float), ("last_skipped", ctypes.c_int32),
                 ("clean", ctypes.c_int64), ("t", ctypes.c_int64),
-                ("skipped_total", ctypes.c_int64)]
+                ("skipped_total", ctypes.c_int64), ("overflows", ctypes.c_int32),
+                ("pad_", ctypes.c_int32)]
 
     def as_tuple(self):
         """(scale, clean, t, skipped_total, last_skipped)."""
@@ -89,7 +94,8 @@ class Decision(ctypes.Structure):
                 ("step_size", ctypes.c_float), ("isb2", ctypes.c_float),
                 ("decay", ctypes.c_float), ("b1", ctypes.c_float),
                 ("omb1", ctypes.c_float), ("b2", ctypes.c_float),
-                ("omb2", ctypes.c_float), ("eps", ctypes.c_float)]
+                ("omb2", ctypes.c_float), ("eps", ctypes.c_float),
+                ("lr", ctypes.c_double)]
 
 
 _P = ctypes.c_void_p
@@ -99,14 +105,18 @@ _I32 = ctypes.c_int32
 
 def hparams(lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=0.0,
             max_grad_norm=0.0, bias_correction=True, dynamic_scale=False,
-            min_scale=1.0, scale_factor=2.0, scale_window=1000) -> Hparams:
+            min_scale=1.0, scale_factor=2.0, scale_window=1000, hysteresis=1,
+            warmup=(0.0, 0.0, 0)) -> Hparams:
+    """`warmup` = (warmup_min_lr, warmup_max_lr, warmup_num_steps); 0 steps
+    keeps lr constant."""
     return Hparams(lr, betas[0], betas[1], eps, weight_decay, max_grad_norm,
                    int(bias_correction), int(dynamic_scale), min_scale,
-                   scale_factor, scale_window)
+                   scale_factor, scale_window, hysteresis, warmup[0], warmup[1],
+                   warmup[2])
 
 
 def scaler(scale: float = 1.0) -> Scaler:
-    return Scaler(scale, 0, 0, 0, 0)
+    return Scaler(scale, 0, 0, 0, 0, 0, 0)
 
 
 def _ptr(a):

@@ -205,9 +205,14 @@ extern "C" orc_stats orc_fold_stats(const orc_stats* per_rank, int32_t n) {
  * lowered when an overflow is detected and raised again once training has
  * been stable; §3.2 gives initial_scale_power 16, loss_scale_window 1000 and
  * min_loss_scale 1.  Reading: an overflowing step is skipped (no state moves,
- * the Adam counter does not advance), the scale is divided by the factor down
- * to the floor and the clean-step counter restarts; after `scale_window`
+ * the Adam counter does not advance) and the clean-step counter restarts; the
+ * scale is divided by the factor (down to the floor) on the `hysteresis`-th
+ * overflow since the scale last changed (§3.2 lists "hysteresis" without a
+ * definition; 1 lowers it on every overflow); after `scale_window`
  * consecutive applied steps the scale is multiplied by the factor.
+ * The learning rate follows WarmupLR (§3.2: warmup_min_lr, warmup_max_lr,
+ * warmup_num_steps; §2.4: the scheduler steps with every parameter update),
+ * read as a linear rise: update t uses min + (max - min) * min(t, T) / T.
  * Clipping divides the unscaled gradient by max(1, norm / max_norm) in the
  * form coef = min(1, max_norm / (norm + 1e-6)).
  * ------------------------------------------------------------------------ */
@@ -222,9 +227,13 @@ extern "C" void orc_decide(const orc_hparams* hp, orc_scaler* st, orc_stats glob
     d->skip = 1;
     d->norm = NAN;
     if (hp->dynamic_scale) {
-      double lowered = (double)scale / hp->scale_factor;
-      if (lowered < hp->min_scale) lowered = hp->min_scale;
-      st->scale = (float)lowered;
+      st->overflows += 1;
+      if (st->overflows >= hp->hysteresis) {
+        double lowered = (double)scale / hp->scale_factor;
+        if (lowered < hp->min_scale) lowered = hp->min_scale;
+        st->scale = (float)lowered;
+        st->overflows = 0;
+      }
     }
     st->clean = 0;
     st->skipped_total += 1;
@@ -248,9 +257,15 @@ extern "C" void orc_decide(const orc_hparams* hp, orc_scaler* st, orc_stats glob
     bc1 = 1.0 - std::pow(hp->beta1, t);
     bc2 = 1.0 - std::pow(hp->beta2, t);
   }
-  d->step_size = (float)(hp->lr / bc1);
+  double lr = hp->lr;
+  if (hp->warmup_num_steps > 0) {
+    const double frac = t < (double)hp->warmup_num_steps ? t / (double)hp->warmup_num_steps : 1.0;
+    lr = hp->warmup_min_lr + (hp->warmup_max_lr - hp->warmup_min_lr) * frac;
+  }
+  d->lr = lr;
+  d->step_size = (float)(lr / bc1);
   d->isb2 = (float)(1.0 / std::sqrt(bc2));
-  d->decay = (float)(1.0 - hp->lr * hp->weight_decay);
+  d->decay = (float)(1.0 - lr * hp->weight_decay);
   d->b1 = (float)hp->beta1;
   d->omb1 = (float)(1.0 - hp->beta1);
   d->b2 = (float)hp->beta2;
@@ -262,6 +277,7 @@ extern "C" void orc_decide(const orc_hparams* hp, orc_scaler* st, orc_stats glob
   if (hp->dynamic_scale && st->clean == hp->scale_window) {
     st->scale = (float)((double)scale * hp->scale_factor);
     st->clean = 0;
+    st->overflows = 0;
   }
 }
 

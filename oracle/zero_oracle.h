@@ -51,6 +51,10 @@ typedef struct orc_hparams {
   double min_scale;            /* floor of the dynamic scale ("min_loss_scale") */
   double scale_factor;         /* 2: halve on overflow, double after window */
   int64_t scale_window;        /* "loss_scale_window" */
+  int64_t hysteresis;          /* overflows that lower the scale once (>= 1) */
+  double warmup_min_lr;        /* WarmupLR: lr of the first update ...          */
+  double warmup_max_lr;        /* ... rising linearly to this one               */
+  int64_t warmup_num_steps;    /* ... over this many updates (0: constant lr)   */
 } orc_hparams;
 
 /* Loss-scaler state of one rank plus the Adam step counter. */
@@ -60,6 +64,8 @@ typedef struct orc_scaler {
   int64_t clean;               /* consecutive clean steps since last change */
   int64_t t;                   /* Adam step counter (updates applied) */
   int64_t skipped_total;
+  int32_t overflows;           /* overflows since the scale last changed */
+  int32_t pad_;
 } orc_scaler;
 
 /* Gradient statistics of one shard (or the fold over all shards). */
@@ -77,6 +83,7 @@ typedef struct orc_decision {
   double inv;                  /* 1 / (scale * divisor) */
   float scale_used;            /* loss scale the gradients were produced with */
   float step_size, isb2, decay, b1, omb1, b2, omb2, eps;
+  double lr;                   /* learning rate of this update */
 } orc_decision;
 
 /* a0: shard bounds.  out = {begin, real_end, shard_len, padded_numel}. */

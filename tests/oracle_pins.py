@@ -591,4 +591,53 @@ def pin_consolidation_is_the_unsharded_state(orc):
     assert (full.view(np.uint32) == ref[0].view(np.uint32)).all()
 
 
+
+
+def pin_hysteresis_schedule(orc):
+    """Hysteresis 2 (tests/golden/loss_scale_hysteresis2.txt); hysteresis 1 is
+    the halve-on-every-overflow rule of the other schedules."""
+    rows = read_golden("loss_scale_hysteresis2.txt")
+    hp = O.hparams(dynamic_scale=True, scale_window=3, min_scale=1.0, hysteresis=2)
+    st = O.scaler(8.0)
+    for step, ev, used, after, ovf in rows:
+        d = orc.decide(hp, st, O.Stats(1.0, 1 if ev == "O" else 0, 0), 1.0)
+        assert d.scale_used == float(used), step
+        assert st.scale == float(after) and st.overflows == int(ovf), step
+    hp1 = O.hparams(dynamic_scale=True, scale_window=1000, hysteresis=1)
+    st = O.scaler(64.0)
+    for k in range(4):
+        orc.decide(hp1, st, O.Stats(1.0, 1, 0), 1.0)
+        assert st.scale == 64.0 / 2 ** (k + 1)
+
+
+def pin_warmup_lr(orc):
+    """WarmupLR with the ds_config.json values ("DeepSpeed tutorial" §3.2:
+    warmup_min_lr 0, warmup_max_lr 2e-5, warmup_num_steps 1000), read as a
+    linear rise over the updates: update t uses 2e-5 * min(t, 1000) / 1000.
+    Skipped steps do not advance it (§2.4: the scheduler steps with every
+    parameter update); with 0 steps the configured lr is used."""
+    hp = O.hparams(lr=5.0, weight_decay=0.5, warmup=(0.0, 2e-5, 1000))
+    st = O.scaler(1.0)
+    seen = {}
+    for k in range(1, 1203):
+        over = (k % 300 == 0)
+        d = orc.decide(hp, st, O.Stats(1.0, int(over), 0), 1.0)
+        if not over:
+            seen[st.t] = (d.lr, d.decay)
+    assert seen[1][0] == 2e-5 * 1 / 1000
+    assert seen[500][0] == 2e-5 * 500 / 1000
+    assert seen[1000][0] == 2e-5 and seen[1198][0] == 2e-5
+    assert seen[1][1] == np.float32(1.0 - 2e-8 * 0.5)
+    hp0 = O.hparams(lr=3e-4, warmup=(0.0, 2e-5, 0))
+    assert orc.decide(hp0, O.scaler(1.0), O.Stats(1.0, 0, 0), 1.0).lr == 3e-4
+    # first update of a warm-up run: the bias-corrected step moves by
+    # -lr_1 * g / (|g| + eps) with lr_1 = max / T
+    hpw = O.hparams(warmup=(1e-3, 1e-2, 4))
+    master, m, v, p16 = _state(8)
+    bufs = [_h(_G8)]
+    g = _f(bufs[0])
+    orc.step(hpw, O.scaler(1.0), bufs, F16, master, m, v, p16, F16, 1.0)
+    _close(master, -(1e-3 + 9e-3 / 4) * g / (np.abs(g) + 1e-8), 2e-6)
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -46,7 +46,8 @@ def test_config_default_is_the_ds_config(z):
     c = z.zero_opt_config_default()
     assert (c.lr, c.beta1, c.beta2, c.eps, c.weight_decay) == (2e-5, 0.9, 0.999, 1e-8, 0.01)
     assert c.init_scale == 2.0 ** 16 and c.scale_window == 1000 and c.min_scale == 1.0
-    assert c.dynamic_scale == 1 and c.hysteresis == 1 and c.bias_correction == 1
+    assert c.dynamic_scale == 1 and c.hysteresis == 2 and c.bias_correction == 1
+    assert c.warmup_num_steps == 0
 
 
 @pytest.mark.parametrize("field,value,status", [
@@ -54,7 +55,8 @@ def test_config_default_is_the_ds_config(z):
     ("lr", -1e-3, 1), ("beta1", 1.0, 1), ("beta2", -0.1, 1), ("eps", 0.0, 1),
     ("weight_decay", -0.5, 1), ("init_scale", 0.0, 1), ("min_scale", -1.0, 1),
     ("scale_factor", 0.5, 1), ("scale_window", 0, 1), ("bias_correction", 2, 1),
-    ("hysteresis", 2, 5), ("max_grad_norm", float("nan"), 1),
+    ("hysteresis", 0, 1), ("max_grad_norm", float("nan"), 1), ("warmup_num_steps", -1, 1),
+    ("warmup_max_lr", -1e-3, 1),
 ])
 def test_create_rejects_bad_config(z, field, value, status):
     cfg = z.make_config(numel=100, world=2)

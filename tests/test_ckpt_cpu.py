@@ -37,7 +37,7 @@ def test_round_trip_is_bit_exact(z, tmp_path):
         assert got.scaler.as_tuple() == info.scaler.as_tuple()
         for a, b in zip(arrs, back):
             assert (a.view(np.uint32) == b.view(np.uint32)).all()
-        assert os.path.getsize(path) == 88 + 12 * n   # header: 8+4+4+8+4+4+8+8+4+4+8+8+8+8
+        assert os.path.getsize(path) == 96 + 12 * n   # header: 8+4+4+8+4+4+8+8+4+4+8+8+8+4+4+8
 
 
 def test_corruption_is_detected(z, tmp_path):

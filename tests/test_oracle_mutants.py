@@ -26,7 +26,7 @@ MUTANTS = [
      "pj = pj - d->step_size * (mj / den);\n    pj = pj * d->decay;"),
     ("decay dropped", "pj = pj * d->decay;", ""),
     ("bias correction exponent t+1", "std::pow(hp->beta1, t)", "std::pow(hp->beta1, t + 1.0)"),
-    ("step size ignores bc1", "(float)(hp->lr / bc1)", "(float)(hp->lr)"),
+    ("step size ignores bc1", "d->step_size = (float)(lr / bc1);", "d->step_size = (float)(lr);"),
     ("isb2 inverted", "(float)(1.0 / std::sqrt(bc2))", "(float)(std::sqrt(bc2))"),
     ("t advances on skipped steps", "st->skipped_total += 1;", "st->skipped_total += 1; st->t += 1;"),
     ("scale grows on overflow", "(double)scale / hp->scale_factor", "(double)scale * hp->scale_factor"),
@@ -46,6 +46,10 @@ MUTANTS = [
     ("bf16 mantissa width", "*mbits = 7; *ebits = 8;", "*mbits = 8; *ebits = 7;"),
     ("shards not padded", "int64_t shard = (numel + world - 1) / world;", "int64_t shard = numel / world;"),
     ("stage 2 keeps full gradients", "case 2: return 2 * psi + 2 * s + 12 * s;", "case 2: return 2 * psi + 2 * psi + 12 * s;"),
+    ("hysteresis ignored", "if (st->overflows >= hp->hysteresis) {", "if (st->overflows >= 1) {"),
+    ("warm-up one update late", "const double frac = t < (double)hp->warmup_num_steps ? t / (double)hp->warmup_num_steps : 1.0;",
+     "const double frac = t - 1.0 < (double)hp->warmup_num_steps ? (t - 1.0) / (double)hp->warmup_num_steps : 1.0;"),
+    ("growth keeps the overflow count", "    st->clean = 0;\n    st->overflows = 0;\n  }", "    st->clean = 0;\n  }"),
     ("16-bit copy in the other format", "p16[j] = orc_f32_to_16(pj, pdtype);",
      "p16[j] = orc_f32_to_16(pj, 1 - pdtype);"),
 ]

@@ -322,3 +322,16 @@ def test_cast_matches_cuda_intrinsics_sample():
         ref = O.f32_to_16(x, O.FP16 if code == z.FP16 else O.BF16)
         assert (got == ref).all()
         z.zero_opt_destroy(h)
+
+
+def test_hysteresis_and_warmup_lr():
+    """Hysteresis 2 (the scale falls on every second overflow) with a WarmupLR
+    schedule (linear over 6 updates) and clipping, 14 steps with overflows on
+    steps 3, 4, 7 and 11; every step's scaler state matches the oracle."""
+    inj = {s: [(0, 1000 + s, INF16)] for s in (3, 4, 7, 11)}
+    case = FlatCase(numel=200_003, world=2, ranks=2, gdtype=O.FP16, lr=1e-3, wd=0.01,
+                    max_norm=0.5, dynamic=True, init_scale=256.0, window=3, hysteresis=2,
+                    warmup=(1e-4, 2e-3, 6), sigma=1e-3, steps=14, inject=inj)
+    res = run_flat(case)
+    assert [h["gpu"][0] for h in res["history"]] == [int(s in inj) for s in range(1, 15)]
+    assert_flat_parity(res)

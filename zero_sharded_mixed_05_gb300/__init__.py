@@ -33,7 +33,8 @@ class zero_opt_config(ctypes.Structure):
                 ("weight_decay", _f64), ("max_grad_norm", _f64),
                 ("dynamic_scale", _i32), ("hysteresis", _i32),
                 ("init_scale", _f64), ("min_scale", _f64), ("scale_factor", _f64),
-                ("scale_window", _i64)]
+                ("scale_window", _i64), ("warmup_min_lr", _f64), ("warmup_max_lr", _f64),
+                ("warmup_num_steps", _i64)]
 
 
 class zero_opt_buffers(ctypes.Structure):
@@ -66,7 +67,8 @@ class zero_opt_step_info(ctypes.Structure):
 
 class zero_opt_scaler_state(ctypes.Structure):
     _fields_ = [("scale", _f32), ("last_skipped", _i32), ("clean_steps", _i64),
-                ("t", _i64), ("skipped_total", _i64)]
+                ("t", _i64), ("skipped_total", _i64), ("overflows", _i32),
+                ("reserved", _i32)]
 
     def as_tuple(self):
         """(scale, clean_steps, t, skipped_total, last_skipped)."""
@@ -186,7 +188,9 @@ def make_config(numel=0, world=1, grad_dtype=FP16, param_dtype=None, lr=2e-5,
                 betas=(0.9, 0.999), eps=1e-8, weight_decay=0.01, max_grad_norm=0.0,
                 bias_correction=True, dynamic_scale=True, init_scale=65536.0,
                 min_scale=1.0, scale_factor=2.0, scale_window=1000,
-                hysteresis=1) -> zero_opt_config:
+                hysteresis=1, warmup=(0.0, 0.0, 0)) -> zero_opt_config:
+    """`warmup` = (warmup_min_lr, warmup_max_lr, warmup_num_steps); 0 steps
+    keeps lr constant."""
     cfg = zero_opt_config()
     _check(lib().zero_opt_config_default(ctypes.byref(cfg)), "zero_opt_config_default")
     cfg.numel = numel
@@ -205,6 +209,7 @@ def make_config(numel=0, world=1, grad_dtype=FP16, param_dtype=None, lr=2e-5,
     cfg.scale_factor = scale_factor
     cfg.scale_window = scale_window
     cfg.hysteresis = hysteresis
+    cfg.warmup_min_lr, cfg.warmup_max_lr, cfg.warmup_num_steps = warmup
     return cfg
 
 

@@ -18,8 +18,8 @@ namespace {
 const char kMagic[8] = {'Z', 'O', 'P', 'T', 'S', 'H', 'D', '1'};
 constexpr uint32_t kVersion = 1;
 // magic, version, reserved, numel, world, rank, begin, real_len, scale,
-// last_skipped, clean_steps, t, skipped_total, checksum
-constexpr long kHeaderBytes = 8 + 4 + 4 + 8 + 4 + 4 + 8 + 8 + 4 + 4 + 8 + 8 + 8 + 8;
+// last_skipped, clean_steps, t, skipped_total, overflows, reserved, checksum
+constexpr long kHeaderBytes = 8 + 4 + 4 + 8 + 4 + 4 + 8 + 8 + 4 + 4 + 8 + 8 + 8 + 4 + 4 + 8;
 
 // 64-bit FNV-1a over 8-byte little-endian words of a byte stream fed in
 // pieces; a trailing partial word is zero-extended.
@@ -138,7 +138,8 @@ zero_status zero_opt_ckpt_write(const char* path, const zero_opt_ckpt_info* info
             put(f.get(), info->begin) && put(f.get(), info->real_len) &&
             put(f.get(), s.scale) && put(f.get(), s.last_skipped) &&
             put(f.get(), s.clean_steps) && put(f.get(), s.t) &&
-            put(f.get(), s.skipped_total) && put(f.get(), sum);
+            put(f.get(), s.skipped_total) && put(f.get(), s.overflows) &&
+            put<int32_t>(f.get(), 0) && put(f.get(), sum);
   ok = ok && write_floats(f.get(), master, info->real_len) &&
        write_floats(f.get(), m, info->real_len) && write_floats(f.get(), v, info->real_len);
   if (!ok) return zo::fail(ZERO_EINVAL, "write to %s failed: %s", path, std::strerror(errno));
@@ -154,6 +155,7 @@ zero_status zero_opt_ckpt_read(const char* path, zero_opt_ckpt_info* info, float
   if (!f) return zo::fail(ZERO_EINVAL, "cannot open %s: %s", path, std::strerror(errno));
   char magic[8];
   uint32_t version = 0, reserved = 0;
+  int32_t reserved2 = 0;
   uint64_t sum = 0;
   zero_opt_ckpt_info in;
   std::memset(&in, 0, sizeof(in));
@@ -164,7 +166,8 @@ zero_status zero_opt_ckpt_read(const char* path, zero_opt_ckpt_info* info, float
                   get(f.get(), &in.begin) && get(f.get(), &in.real_len) &&
                   get(f.get(), &s.scale) && get(f.get(), &s.last_skipped) &&
                   get(f.get(), &s.clean_steps) && get(f.get(), &s.t) &&
-                  get(f.get(), &s.skipped_total) && get(f.get(), &sum);
+                  get(f.get(), &s.skipped_total) && get(f.get(), &s.overflows) &&
+                  get(f.get(), &reserved2) && get(f.get(), &sum);
   if (!ok) return zo::fail(ZERO_EINVAL, "%s: truncated header", path);
   if (std::memcmp(magic, kMagic, 8) != 0) return zo::fail(ZERO_EINVAL, "%s: not a shard file", path);
   if (version != kVersion) return zo::fail(ZERO_EINVAL, "%s: unknown version %u", path, version);

@@ -309,8 +309,9 @@ __device__ __forceinline__ double block_sum(double x, double* red) {
 
 // ------------------------------------------------------------- decisions (a4)
 // Run by one thread of the last CTA.  Scalars are computed in binary64 and
-// rounded once to binary32.  Overflow: skip, scale /= factor (not below
-// min_scale), clean count restarts.  Otherwise: norm of the unscaled gradient,
+// rounded once to binary32.  Overflow: skip, clean count restarts, and on the
+// hysteresis-th overflow since the scale last changed scale /= factor (not
+// below min_scale).  The update's lr is lr, or WarmupLR's linear value.  Otherwise: norm of the unscaled gradient,
 // clip coefficient min(1, max_norm / (norm + 1e-6)), Adam step t += 1 with its
 // bias corrections, and the scale grows by the factor after `window`
 // consecutive applied steps.
@@ -358,9 +359,13 @@ static __device__ void decide(const Pass1Args& a, double own_sumsq, int own_flag
     d.skip = 1;
     d.norm = __longlong_as_double(0x7ff8000000000000ll);
     if (a.hp.dynamic) {
-      double lowered = (double)scale / a.hp.factor;
-      if (lowered < a.hp.min_scale) lowered = a.hp.min_scale;
-      st.scale = (float)lowered;
+      st.overflows += 1;
+      if (st.overflows >= a.hp.hysteresis) {
+        double lowered = (double)scale / a.hp.factor;
+        if (lowered < a.hp.min_scale) lowered = a.hp.min_scale;
+        st.scale = (float)lowered;
+        st.overflows = 0;
+      }
     }
     st.clean = 0;
     st.skipped_total += 1;
@@ -381,9 +386,16 @@ static __device__ void decide(const Pass1Args& a, double own_sumsq, int own_flag
       bc1 = 1.0 - pow(a.hp.beta1, (double)st.t);
       bc2 = 1.0 - pow(a.hp.beta2, (double)st.t);
     }
-    d.step_size = (float)(a.hp.lr / bc1);
+    double lr = a.hp.lr;
+    if (a.hp.warmup_num_steps > 0) {
+      const double T = (double)a.hp.warmup_num_steps;
+      const double t = (double)st.t;
+      const double frac = t < T ? t / T : 1.0;
+      lr = a.hp.warmup_min_lr + (a.hp.warmup_max_lr - a.hp.warmup_min_lr) * frac;
+    }
+    d.step_size = (float)(lr / bc1);
     d.isb2 = (float)(1.0 / sqrt(bc2));
-    d.decay = (float)(1.0 - a.hp.lr * a.hp.wd);
+    d.decay = (float)(1.0 - lr * a.hp.wd);
     d.b1 = (float)a.hp.beta1;
     d.omb1 = (float)(1.0 - a.hp.beta1);
     d.b2 = (float)a.hp.beta2;
@@ -394,6 +406,7 @@ static __device__ void decide(const Pass1Args& a, double own_sumsq, int own_flag
     if (a.hp.dynamic && st.clean == a.hp.window) {
       st.scale = (float)((double)scale * a.hp.factor);
       st.clean = 0;
+      st.overflows = 0;
     }
   }
   d.t = st.t;

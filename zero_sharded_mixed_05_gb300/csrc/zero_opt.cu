@@ -132,7 +132,9 @@ zero_status check_config(const zero_opt_config* c) {
     return fail(ZERO_EINVAL, "bias_correction must be 0 or 1");
   if (c->dynamic_scale != 0 && c->dynamic_scale != 1)
     return fail(ZERO_EINVAL, "dynamic_scale must be 0 or 1");
-  if (c->hysteresis != 1) return fail(ZERO_ENOTSUP, "hysteresis must be 1");
+  if (c->hysteresis < 1) return fail(ZERO_EINVAL, "hysteresis must be >= 1");
+  if (c->warmup_num_steps < 0 || !(c->warmup_min_lr >= 0.0) || !(c->warmup_max_lr >= 0.0))
+    return fail(ZERO_EINVAL, "warm-up steps and learning rates must be >= 0");
   return ZERO_OK;
 }
 
@@ -306,6 +308,10 @@ zo::Hyper hyper_of(const zero_opt_config& c, double divisor) {
   hp.window = c.scale_window;
   hp.bias_correction = c.bias_correction;
   hp.dynamic = c.dynamic_scale;
+  hp.hysteresis = c.hysteresis;
+  hp.warmup_min_lr = c.warmup_min_lr;
+  hp.warmup_max_lr = c.warmup_max_lr;
+  hp.warmup_num_steps = c.warmup_num_steps;
   return hp;
 }
 
@@ -503,7 +509,7 @@ zero_status zero_opt_config_default(zero_opt_config* c) {
   c->weight_decay = 0.01;
   c->max_grad_norm = 0.0;
   c->dynamic_scale = 1;
-  c->hysteresis = 1;
+  c->hysteresis = 2;
   c->init_scale = 65536.0;
   c->min_scale = 1.0;
   c->scale_factor = 2.0;
@@ -549,6 +555,8 @@ zero_status zero_opt_create(const zero_opt_config* cfg, zero_opt_t* out) {
     r0[r].clean = 0;
     r0[r].t = 0;
     r0[r].skipped_total = 0;
+    r0[r].overflows = 0;
+    r0[r].reserved = 0;
   }
   e = cudaMemcpy(ws, init.data(), ws_bytes, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMallocHost(&h->pinned, kPinnedBytes);
@@ -725,7 +733,8 @@ zero_status zero_opt_set_loss_scale(zero_opt_t h, int32_t rank, void* stream,
   zero_status st = check_handle_rank(h, rank);
   if (st != ZERO_OK) return st;
   if (!in) return fail(ZERO_EINVAL, "in is NULL");
-  if (!(in->scale > 0.0f) || in->clean_steps < 0 || in->t < 0 || in->skipped_total < 0)
+  if (!(in->scale > 0.0f) || in->clean_steps < 0 || in->t < 0 || in->skipped_total < 0 ||
+      in->overflows < 0)
     return fail(ZERO_EINVAL, "scale must be > 0 and counters >= 0");
   st = check_device(h);
   if (st != ZERO_OK) return st;

@@ -37,6 +37,8 @@ struct RankState {
   int64_t clean;
   int64_t t;
   int64_t skipped_total;
+  int32_t overflows;     // overflows since the scale last changed
+  int32_t reserved;
 };
 static_assert(sizeof(RankState) == sizeof(zero_opt_scaler_state), "layout");
 
@@ -71,6 +73,9 @@ struct Hyper {
   double lr, beta1, beta2, eps, wd, max_norm, divisor, min_scale, factor;
   int64_t window;
   int32_t bias_correction, dynamic;
+  int64_t hysteresis;
+  double warmup_min_lr, warmup_max_lr;
+  int64_t warmup_num_steps;
 };
 
 enum Mode : int32_t { kStepLocal = 0, kStepGlobal = 1, kStatsOnly = 2 };
