@@ -410,6 +410,51 @@ zero_status zero_opt_grad_stats_noalloc(const void* const* grads, int32_t n_bufs
                                         int32_t grad_dtype, int64_t n, void* stream,
                                         zero_opt_stats* out);
 
+/* ---------------------------------------------------------------------------
+ * Offloaded step: the same per-shard step on HOST-resident state, computed by
+ * a pool of CPU threads ("DeepSpeed tutorial" §4.3 CPU offload and
+ * "DeepSpeed ZeRO引擎深入" 卸载策略: the optimizer states, and the
+ * gradients, live in CPU memory and the update runs there, trading transfer
+ * time for device memory).  No CUDA call is made; these functions work on a
+ * machine without a GPU.  The results are those of zero_opt_step on the same
+ * inputs: the same binary32 operation sequence per element, the same 16-bit
+ * rounding, the same decisions (one shared implementation) and the same loss
+ * scale sequence; only the sum of squares may differ from the device's in the
+ * last bits of its binary64 value (both are compensated sums).
+ *
+ * zero_host_create: `n_threads` worker threads (<= 0: the number of hardware
+ * threads; at most 1024), started here and kept until zero_host_destroy.
+ * The handle keeps one loss-scaler replica per rank, initialised as
+ * zero_opt_create does.  Errors: EINVAL (NULL cfg/out, invalid config),
+ * ENOMEM.
+ *
+ * Buffers are zero_opt_buffers whose pointers are all HOST pointers (the
+ * grads array and every gradient buffer, master, m, v, param16) with the same
+ * meaning, lengths and indexing as for zero_opt_step; `stash` is ignored (the
+ * sums are recomputed).  Calls on one handle must not overlap; the caller's
+ * buffers must not be touched by other threads during a call.
+ *
+ * zero_host_grad_stats: statistics of the rank's shard (for a fold over ranks
+ * with zero_opt_fold_stats).  zero_host_step: the step of `rank`; `global` as
+ * in zero_opt_step (NULL: this shard's own statistics).  Both return when the
+ * work is done.  zero_host_loss_scale / zero_host_set_loss_scale read and
+ * replace a rank's scaler replica; zero_host_last_step reports the last step
+ * of any rank.  Errors: EINVAL (NULL handle/buffers/pointer, R*K < 1),
+ * ERANGE (rank outside [0, world), R*K > 1024). */
+typedef struct zero_host_handle* zero_host_t;
+
+zero_status zero_host_create(const zero_opt_config* cfg, int32_t n_threads, zero_host_t* out);
+zero_status zero_host_destroy(zero_host_t h);
+zero_status zero_host_threads(zero_host_t h, int32_t* n_threads);
+zero_status zero_host_grad_stats(zero_host_t h, int32_t rank, const zero_opt_buffers* bufs,
+                                 zero_opt_stats* out);
+zero_status zero_host_step(zero_host_t h, int32_t rank, const zero_opt_buffers* bufs,
+                           const zero_opt_stats* global);
+zero_status zero_host_loss_scale(zero_host_t h, int32_t rank, zero_opt_scaler_state* out);
+zero_status zero_host_set_loss_scale(zero_host_t h, int32_t rank,
+                                     const zero_opt_scaler_state* state);
+zero_status zero_host_last_step(zero_host_t h, zero_opt_step_info* out);
+
 /* Static string describing a status code; never NULL. */
 const char* zero_opt_status_string(zero_status s);
 

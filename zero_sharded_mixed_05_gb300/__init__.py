@@ -119,6 +119,14 @@ SIGNATURES = [
     ("zero_opt_load_shard", _i32, [_vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp, ctypes.c_char_p]),
     ("zero_opt_consolidate_fp32", _i32, [_P(ctypes.c_char_p), _i32, _i64, _vp]),
     ("zero_opt_grad_stats_noalloc", _i32, [_P(_vp), _i32, _i32, _i64, _vp, _vp]),
+    ("zero_host_create", _i32, [_P(zero_opt_config), _i32, _P(_vp)]),
+    ("zero_host_destroy", _i32, [_vp]),
+    ("zero_host_threads", _i32, [_vp, _P(_i32)]),
+    ("zero_host_grad_stats", _i32, [_vp, _i32, _P(zero_opt_buffers), _P(zero_opt_stats)]),
+    ("zero_host_step", _i32, [_vp, _i32, _P(zero_opt_buffers), _P(zero_opt_stats)]),
+    ("zero_host_loss_scale", _i32, [_vp, _i32, _P(zero_opt_scaler_state)]),
+    ("zero_host_set_loss_scale", _i32, [_vp, _i32, _P(zero_opt_scaler_state)]),
+    ("zero_host_last_step", _i32, [_vp, _P(zero_opt_step_info)]),
     ("zero_opt_status_string", ctypes.c_char_p, [_i32]),
     ("zero_opt_last_error", ctypes.c_char_p, []),
 ]
@@ -150,11 +158,14 @@ def _check(status: int, where: str) -> None:
 
 
 def _ptr(x):
+    """Address of a torch tensor or numpy array (or an int address)."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
-    return x.data_ptr()
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    return x.ctypes.data
 
 
 def current_stream(device=None) -> int:
@@ -453,3 +464,52 @@ def zero_opt_grad_stats_noalloc(grads, grad_dtype: int, n: int, out, stream=None
     _check(lib().zero_opt_grad_stats_noalloc(ctypes.cast(arr, _P(_vp)), len(grads), grad_dtype,
                                              n, _stream(stream), _ptr(out)),
            "zero_opt_grad_stats_noalloc")
+
+
+# ---------------------------------------------------------------- offloaded (host) step
+# Same calls on host-resident buffers (numpy arrays or CPU tensors); no GPU.
+
+def zero_host_create(cfg: zero_opt_config, n_threads: int = 0) -> int:
+    h = _vp()
+    _check(lib().zero_host_create(ctypes.byref(cfg), n_threads, ctypes.byref(h)),
+           "zero_host_create")
+    return h.value
+
+
+def zero_host_destroy(h) -> None:
+    _check(lib().zero_host_destroy(h), "zero_host_destroy")
+
+
+def zero_host_threads(h) -> int:
+    n = _i32()
+    _check(lib().zero_host_threads(h, ctypes.byref(n)), "zero_host_threads")
+    return n.value
+
+
+def zero_host_grad_stats(h, rank: int, bufs: zero_opt_buffers) -> zero_opt_stats:
+    out = zero_opt_stats()
+    _check(lib().zero_host_grad_stats(h, rank, ctypes.byref(bufs), ctypes.byref(out)),
+           "zero_host_grad_stats")
+    return out
+
+
+def zero_host_step(h, rank: int, bufs: zero_opt_buffers, global_stats=None) -> None:
+    gs = ctypes.byref(global_stats) if global_stats is not None else None
+    _check(lib().zero_host_step(h, rank, ctypes.byref(bufs), gs), "zero_host_step")
+
+
+def zero_host_loss_scale(h, rank: int) -> zero_opt_scaler_state:
+    out = zero_opt_scaler_state()
+    _check(lib().zero_host_loss_scale(h, rank, ctypes.byref(out)), "zero_host_loss_scale")
+    return out
+
+
+def zero_host_set_loss_scale(h, rank: int, state: zero_opt_scaler_state) -> None:
+    _check(lib().zero_host_set_loss_scale(h, rank, ctypes.byref(state)),
+           "zero_host_set_loss_scale")
+
+
+def zero_host_last_step(h) -> zero_opt_step_info:
+    out = zero_opt_step_info()
+    _check(lib().zero_host_last_step(h, ctypes.byref(out)), "zero_host_last_step")
+    return out

@@ -11,9 +11,9 @@ ROOT = os.path.dirname(PKG)
 INCLUDE = os.path.join(ROOT, "include")
 CSRC = os.path.join(PKG, "csrc")
 SOURCES = [os.path.join(CSRC, "zero_opt.cu"), os.path.join(CSRC, "ckpt.cpp"),
-           os.path.join(CSRC, "noalloc.cu")]
+           os.path.join(CSRC, "noalloc.cu"), os.path.join(CSRC, "host_step.cpp")]
 DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("kernels.cuh", "zero_opt_internal.h",
-                                                     "host_util.h")] + [
+                                                     "host_util.h", "decide_core.h")] + [
     os.path.join(INCLUDE, "zero_opt.h")]
 LIB = os.path.join(PKG, "libzero_opt.so")
 
@@ -22,7 +22,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # binary64 per-step scalars round exactly like the host definition; the
 # per-element binary32 update uses explicit _rn intrinsics regardless.
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-fmad=false",
-                     "-Xcompiler", "-fPIC,-O2,-ffp-contract=off",
+                     "-Xcompiler", "-fPIC,-O3,-ffp-contract=off,-fno-math-errno",
                      "-I", INCLUDE]
 
 

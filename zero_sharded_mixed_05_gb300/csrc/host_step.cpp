@@ -1,0 +1,482 @@
+// host_step.cpp -- the offloaded optimizer step: the per-shard step of
+// zero_opt_step (reduce, overflow flag, sum of squares, decision, AdamW,
+// 16-bit write-back) on host-resident buffers, computed by a pool of CPU
+// threads.  Sources: "DeepSpeed tutorial" §4.3 (ZeRO-Offload keeps the
+// optimizer states and gradients in CPU memory) and "DeepSpeed ZeRO引擎深入"
+// 卸载策略 (the update moves to the CPU to relieve device memory).
+//
+// Work split: the shard's real elements are cut into one contiguous range per
+// thread (multiples of kBlock elements).  Each thread reduces its range block
+// by block in buffer order, and either accumulates the squares (statistics)
+// or applies the update.  Partial sums of squares are folded in thread
+// order, so a result depends only on the inputs and the thread count.
+//
+// Every binary32 operation of the update is a separate IEEE operation in
+// round-to-nearest: this file is compiled without floating-point contraction
+// (-ffp-contract=off) and without any fast-math option, so vectorised code
+// computes exactly what the scalar source says.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <condition_variable>
+#include <cstdint>
+#include <cstring>
+#include <functional>
+#include <mutex>
+#include <new>
+#include <thread>
+#include <vector>
+
+#include "decide_core.h"
+#include "host_util.h"
+#include "zero_opt.h"
+#include "zero_opt_internal.h"
+
+namespace {
+
+using zo::fail;
+
+constexpr int64_t kBlock = 1024;  // elements reduced at a time per thread
+constexpr int kMaxThreads = 1024;
+
+// ------------------------------------------------------------------ threads
+// A fixed set of workers; run(f) calls f(i) for i in [0, n) -- i = 0 on the
+// calling thread -- and returns when every call has returned.
+class Pool {
+ public:
+  explicit Pool(int n) : n_(n) {
+    for (int i = 1; i < n; ++i) workers_.emplace_back([this, i] { loop(i); });
+  }
+  ~Pool() {
+    {
+      std::lock_guard<std::mutex> l(mu_);
+      stop_ = true;
+    }
+    cv_.notify_all();
+    for (auto& t : workers_) t.join();
+  }
+  int size() const { return n_; }
+  void run(const std::function<void(int)>& f) {
+    {
+      std::lock_guard<std::mutex> l(mu_);
+      job_ = &f;
+      pending_ = n_ - 1;
+      ++gen_;
+    }
+    cv_.notify_all();
+    f(0);
+    std::unique_lock<std::mutex> l(mu_);
+    done_.wait(l, [this] { return pending_ == 0; });
+    job_ = nullptr;
+  }
+
+ private:
+  void loop(int i) {
+    uint64_t seen = 0;
+    for (;;) {
+      const std::function<void(int)>* job;
+      {
+        std::unique_lock<std::mutex> l(mu_);
+        cv_.wait(l, [&] { return stop_ || gen_ != seen; });
+        if (stop_) return;
+        seen = gen_;
+        job = job_;
+      }
+      (*job)(i);
+      std::lock_guard<std::mutex> l(mu_);
+      if (--pending_ == 0) done_.notify_one();
+    }
+  }
+  int n_;
+  std::vector<std::thread> workers_;
+  std::mutex mu_;
+  std::condition_variable cv_, done_;
+  const std::function<void(int)>* job_ = nullptr;
+  uint64_t gen_ = 0;
+  int pending_ = 0;
+  bool stop_ = false;
+};
+
+// ------------------------------------------------------------------ 16-bit formats
+// IEEE binary16 to binary32 for all 65536 patterns (exact; NaN payloads kept).
+struct HalfTable {
+  float v[65536];
+  HalfTable() {
+    for (uint32_t h = 0; h < 65536; ++h) {
+      const uint32_t sign = (h & 0x8000u) << 16;
+      const uint32_t e = (h >> 10) & 0x1fu, f = h & 0x3ffu;
+      float x;
+      if (e == 0) {
+        x = (float)f * 0x1p-24f;  // zero or subnormal: f * 2^-24, exact
+        uint32_t b;
+        std::memcpy(&b, &x, 4);
+        b |= sign;
+        std::memcpy(&x, &b, 4);
+      } else {
+        const uint32_t b = sign | (e == 31 ? (0xffu << 23) | (f << 13)
+                                           : ((e + 112u) << 23) | (f << 13));
+        std::memcpy(&x, &b, 4);
+      }
+      v[h] = x;
+    }
+  }
+};
+const HalfTable& half_table() {
+  static const HalfTable* t = new HalfTable();
+  return *t;
+}
+
+inline float bf16_to_f32(uint16_t h) {
+  const uint32_t b = (uint32_t)h << 16;
+  float x;
+  std::memcpy(&x, &b, 4);
+  return x;
+}
+
+// The two casts below are written without branches (every case computed,
+// then selected) so that the compiler can vectorise the loops that use them.
+
+inline uint32_t bits_of(float x) {
+  uint32_t b;
+  std::memcpy(&b, &x, 4);
+  return b;
+}
+inline float float_of(uint32_t b) {
+  float x;
+  std::memcpy(&x, &b, 4);
+  return x;
+}
+
+// binary32 to bfloat16, round to nearest even; NaN stays a (quiet) NaN.
+inline uint16_t f32_to_bf16(float x) {
+  const uint32_t b = bits_of(x);
+  const uint32_t rounded = (b + 0x7fffu + ((b >> 16) & 1u)) >> 16;
+  const uint32_t quiet = (b >> 16) | 0x40u;
+  return (uint16_t)((b & 0x7fffffffu) > 0x7f800000u ? quiet : rounded);
+}
+
+// binary32 to binary16, round to nearest even, overflow to infinity, NaN to
+// the quiet NaN 0x7e00 (with the sign).
+inline uint16_t f32_to_f16(float x) {
+  const uint32_t b = bits_of(x);
+  const uint32_t sign = (b >> 16) & 0x8000u;
+  const uint32_t a = b & 0x7fffffffu;
+  // normal results: round the 23-bit fraction at bit 13, rebias 127 -> 15
+  const uint32_t normal = (a + 0xfffu + ((a >> 13) & 1u) - (112u << 23)) >> 13;
+  // below 2^-14 the result is a multiple of 2^-24: |x| * 2^24 < 1024 is
+  // exact, and adding then removing 2^23 rounds it to an integer (RNE)
+  const float f = float_of(a < 0x38800000u ? a : 0x38800000u);
+  const uint32_t sub = (uint32_t)(int32_t)((f * 0x1p24f + 0x1p23f) - 0x1p23f);
+  uint32_t r = a < 0x38800000u ? sub : normal;
+  r = a >= 0x477ff000u ? 0x7c00u : r;  // >= 65520 rounds to infinity (and inf)
+  r = a > 0x7f800000u ? 0x7e00u : r;   // NaN
+  return (uint16_t)(sign | r);
+}
+
+// ------------------------------------------------------------------ sums of squares
+// Compensated binary64 accumulation in four independent lanes (Knuth's
+// TwoSum on each addition): the lanes' error terms keep the sum of the exact
+// binary64 squares to far below binary64 precision.
+struct SqSum {
+  double hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};
+  static inline void two_sum(double& hi, double& lo, double x) {
+    const double t = hi + x;
+    const double bp = t - hi;
+    lo += (hi - (t - bp)) + (x - bp);
+    hi = t;
+  }
+  void add_block(const float* s, int64_t n) {
+    int64_t j = 0;
+    for (; j + 4 <= n; j += 4)
+      for (int l = 0; l < 4; ++l) two_sum(hi[l], lo[l], (double)s[j + l] * (double)s[j + l]);
+    for (; j < n; ++j) two_sum(hi[0], lo[0], (double)s[j] * (double)s[j]);
+  }
+  // fold into (h, l) in lane order
+  void into(double& h, double& l) const {
+    for (int k = 0; k < 4; ++k) {
+      two_sum(h, l, hi[k]);
+      two_sum(h, l, lo[k]);
+    }
+  }
+};
+
+// ------------------------------------------------------------------ the step
+struct Job {
+  const zero_opt_config* cfg;
+  const uint16_t* const* g;  // per buffer: first element of the shard
+  int nbuf;
+  int64_t n;                 // real elements of the shard
+  float* master;
+  float* m;
+  float* v;
+  uint16_t* p16;             // first element of the shard
+};
+
+// Reduced binary32 sums of elements [j0, j0 + len) in buffer order.
+inline void reduce_block(const Job& jb, int64_t j0, int64_t len, float* s) {
+  const bool half = jb.cfg->grad_dtype == ZERO_FP16;
+  const float* tab = half ? half_table().v : nullptr;
+  for (int64_t k = 0; k < len; ++k) s[k] = 0.0f;
+  for (int b = 0; b < jb.nbuf; ++b) {
+    const uint16_t* g = jb.g[b] + j0;
+    if (half) {
+      for (int64_t k = 0; k < len; ++k) s[k] = s[k] + tab[g[k]];
+    } else {
+      for (int64_t k = 0; k < len; ++k) s[k] = s[k] + bf16_to_f32(g[k]);
+    }
+  }
+}
+
+void range_of(const Job& jb, int nt, int i, int64_t* lo, int64_t* hi) {
+  const int64_t blocks = (jb.n + kBlock - 1) / kBlock;
+  const int64_t per = (blocks + nt - 1) / nt;
+  *lo = std::min(jb.n, (int64_t)i * per * kBlock);
+  *hi = std::min(jb.n, (int64_t)(i + 1) * per * kBlock);
+}
+
+struct Partial {
+  double hi = 0.0, lo = 0.0;
+  int nonfinite = 0;
+  char pad[64 - 2 * sizeof(double) - sizeof(int)];
+};
+
+void stats_range(const Job& jb, int64_t lo, int64_t hi, Partial* out) {
+  alignas(64) float s[kBlock];
+  SqSum acc;
+  int bad = 0;
+  for (int64_t j0 = lo; j0 < hi; j0 += kBlock) {
+    const int64_t len = std::min(kBlock, hi - j0);
+    reduce_block(jb, j0, len, s);
+    for (int64_t k = 0; k < len; ++k) bad |= !(std::fabs(s[k]) <= 3.40282347e38f);
+    acc.add_block(s, len);
+  }
+  acc.into(out->hi, out->lo);
+  out->nonfinite = bad;
+}
+
+void update_range(const Job& jb, const zo::Decision& d, int64_t lo, int64_t hi) {
+  alignas(64) float s[kBlock];
+  const bool half16 = jb.cfg->param_dtype == ZERO_FP16;
+  const float coef = d.coef, b1 = d.b1, omb1 = d.omb1, b2 = d.b2, omb2 = d.omb2;
+  const float isb2 = d.isb2, eps = d.eps, decay = d.decay, step_size = d.step_size;
+  for (int64_t j0 = lo; j0 < hi; j0 += kBlock) {
+    const int64_t len = std::min(kBlock, hi - j0);
+    reduce_block(jb, j0, len, s);
+    float* __restrict__ P = jb.master + j0;
+    float* __restrict__ M = jb.m + j0;
+    float* __restrict__ V = jb.v + j0;
+    uint16_t* __restrict__ Q = jb.p16 + j0;
+    for (int64_t k = 0; k < len; ++k) {
+      const float g = s[k] * coef;
+      const float mk = b1 * M[k] + omb1 * g;
+      const float vk = b2 * V[k] + omb2 * (g * g);
+      const float den = std::sqrt(vk) * isb2 + eps;
+      float p = P[k] * decay;
+      p = p - step_size * (mk / den);
+      M[k] = mk;
+      V[k] = vk;
+      P[k] = p;
+    }
+    if (half16) {
+      for (int64_t k = 0; k < len; ++k) Q[k] = f32_to_f16(P[k]);
+    } else {
+      for (int64_t k = 0; k < len; ++k) Q[k] = f32_to_bf16(P[k]);
+    }
+  }
+}
+
+}  // namespace
+
+struct zero_host_handle {
+  zero_opt_config cfg;
+  std::vector<zo::RankState> ranks;
+  zo::Decision last;
+  Pool* pool = nullptr;
+};
+
+namespace {
+
+zero_status check_rank(zero_host_t h, int32_t rank) {
+  if (!h) return fail(ZERO_EINVAL, "handle is NULL");
+  if (rank < 0 || rank >= h->cfg.world)
+    return fail(ZERO_ERANGE, "rank %d outside [0, %d)", rank, h->cfg.world);
+  return ZERO_OK;
+}
+
+// Validate `b` and describe the rank's shard as a Job.
+zero_status make_job(zero_host_t h, int32_t rank, const zero_opt_buffers* b, bool need_state,
+                     std::vector<const uint16_t*>* g, Job* jb) {
+  zero_status st = check_rank(h, rank);
+  if (st != ZERO_OK) return st;
+  if (!b) return fail(ZERO_EINVAL, "buffers is NULL");
+  if (b->n_ranks < 1 || b->n_micro < 1) return fail(ZERO_EINVAL, "n_ranks and n_micro must be >= 1");
+  const int64_t nbuf = (int64_t)b->n_ranks * b->n_micro;
+  if (nbuf > zo::kMaxBufs)
+    return fail(ZERO_ERANGE, "n_ranks*n_micro = %lld exceeds %d", (long long)nbuf, zo::kMaxBufs);
+  if (!b->grads) return fail(ZERO_EINVAL, "grads array is NULL");
+  int64_t begin, real, S;
+  zo::shard_range(h->cfg.numel, h->cfg.world, rank, &begin, &real, &S);
+  if (real > 0) {
+    for (int64_t k = 0; k < nbuf; ++k)
+      if (!b->grads[k]) return fail(ZERO_EINVAL, "gradient pointer %lld is NULL", (long long)k);
+    if (need_state && (!b->master || !b->m || !b->v || !b->param16))
+      return fail(ZERO_EINVAL, "master, m, v and param16 must not be NULL");
+  }
+  g->resize((size_t)nbuf);
+  const int64_t goff = b->grads_shard_local ? 0 : begin;
+  for (int64_t k = 0; k < nbuf; ++k)
+    (*g)[k] = b->grads[k] ? static_cast<const uint16_t*>(b->grads[k]) + goff : nullptr;
+  jb->cfg = &h->cfg;
+  jb->g = g->data();
+  jb->nbuf = (int)nbuf;
+  jb->n = real;
+  jb->master = b->master;
+  jb->m = b->m;
+  jb->v = b->v;
+  jb->p16 = b->param16 ? static_cast<uint16_t*>(b->param16) + (b->param16_shard_local ? 0 : begin)
+                       : nullptr;
+  return ZERO_OK;
+}
+
+zero_opt_stats shard_stats(zero_host_t h, const Job& jb) {
+  const int nt = h->pool->size();
+  std::vector<Partial> part((size_t)nt);
+  h->pool->run([&](int i) {
+    int64_t lo, hi;
+    range_of(jb, nt, i, &lo, &hi);
+    stats_range(jb, lo, hi, &part[(size_t)i]);
+  });
+  double H = 0.0, L = 0.0;
+  int bad = 0;
+  for (const Partial& p : part) {
+    SqSum::two_sum(H, L, p.hi);
+    SqSum::two_sum(H, L, p.lo);
+    bad |= p.nonfinite;
+  }
+  zero_opt_stats out;
+  out.sumsq = H + L;
+  out.nonfinite = bad;
+  out.reserved = 0;
+  return out;
+}
+
+}  // namespace
+
+extern "C" {
+
+zero_status zero_host_create(const zero_opt_config* cfg, int32_t n_threads, zero_host_t* out) {
+  if (!cfg || !out) return fail(ZERO_EINVAL, "cfg and out must not be NULL");
+  zero_status st = zo::check_config(cfg);
+  if (st != ZERO_OK) return st;
+  int n = n_threads;
+  if (n <= 0) n = (int)std::max(1u, std::thread::hardware_concurrency());
+  n = std::min(n, kMaxThreads);
+  zero_host_t h = new (std::nothrow) zero_host_handle();
+  if (!h) return fail(ZERO_ENOMEM, "host handle");
+  try {
+    h->cfg = *cfg;
+    h->ranks.resize((size_t)cfg->world);
+    for (auto& r : h->ranks) {
+      r.scale = (float)cfg->init_scale;
+      r.last_skipped = 0;
+      r.clean = 0;
+      r.t = 0;
+      r.skipped_total = 0;
+      r.overflows = 0;
+      r.reserved = 0;
+    }
+    std::memset(&h->last, 0, sizeof(h->last));
+    half_table();
+    h->pool = new Pool(n);
+  } catch (...) {
+    delete h;
+    return fail(ZERO_ENOMEM, "host handle: allocation or thread start failed");
+  }
+  *out = h;
+  return ZERO_OK;
+}
+
+zero_status zero_host_destroy(zero_host_t h) {
+  if (!h) return fail(ZERO_EINVAL, "handle is NULL");
+  delete h->pool;
+  delete h;
+  return ZERO_OK;
+}
+
+zero_status zero_host_threads(zero_host_t h, int32_t* n_threads) {
+  if (!h || !n_threads) return fail(ZERO_EINVAL, "NULL argument");
+  *n_threads = h->pool->size();
+  return ZERO_OK;
+}
+
+zero_status zero_host_grad_stats(zero_host_t h, int32_t rank, const zero_opt_buffers* bufs,
+                                 zero_opt_stats* out) {
+  if (!out) return fail(ZERO_EINVAL, "out is NULL");
+  std::vector<const uint16_t*> g;
+  Job jb;
+  zero_status st = make_job(h, rank, bufs, false, &g, &jb);
+  if (st != ZERO_OK) return st;
+  *out = shard_stats(h, jb);
+  return ZERO_OK;
+}
+
+zero_status zero_host_step(zero_host_t h, int32_t rank, const zero_opt_buffers* bufs,
+                           const zero_opt_stats* global) {
+  std::vector<const uint16_t*> g;
+  Job jb;
+  zero_status st = make_job(h, rank, bufs, true, &g, &jb);
+  if (st != ZERO_OK) return st;
+  zero_opt_stats s;
+  if (global) {
+    s = *global;
+  } else {
+    s = shard_stats(h, jb);
+  }
+  const double divisor =
+      bufs->divisor > 0.0 ? bufs->divisor : (double)bufs->n_ranks * (double)bufs->n_micro;
+  const zo::Hyper hp = zo::hyper_of(h->cfg, divisor);
+  zo::RankState& rs = h->ranks[(size_t)rank];
+  const zo::Decision d =
+      zo::decide_core(hp, rs, s.sumsq, s.nonfinite ? 1 : 0,
+                      [&hp](int64_t t, float* ss, float* isb2, float* decay) {
+                        zo::step_scalars(hp, t, ss, isb2, decay);
+                      });
+  h->last = d;
+  if (!d.skip && jb.n > 0) {
+    const int nt = h->pool->size();
+    h->pool->run([&](int i) {
+      int64_t lo, hi;
+      range_of(jb, nt, i, &lo, &hi);
+      update_range(jb, d, lo, hi);
+    });
+  }
+  return ZERO_OK;
+}
+
+zero_status zero_host_loss_scale(zero_host_t h, int32_t rank, zero_opt_scaler_state* out) {
+  zero_status st = check_rank(h, rank);
+  if (st != ZERO_OK) return st;
+  if (!out) return fail(ZERO_EINVAL, "out is NULL");
+  std::memcpy(out, &h->ranks[(size_t)rank], sizeof(*out));
+  return ZERO_OK;
+}
+
+zero_status zero_host_set_loss_scale(zero_host_t h, int32_t rank,
+                                     const zero_opt_scaler_state* state) {
+  zero_status st = check_rank(h, rank);
+  if (st != ZERO_OK) return st;
+  if (!state) return fail(ZERO_EINVAL, "state is NULL");
+  if (!(state->scale > 0.0f) || state->clean_steps < 0 || state->t < 0 ||
+      state->skipped_total < 0 || state->overflows < 0)
+    return fail(ZERO_EINVAL, "scale must be > 0 and the counters >= 0");
+  std::memcpy(&h->ranks[(size_t)rank], state, sizeof(*state));
+  return ZERO_OK;
+}
+
+zero_status zero_host_last_step(zero_host_t h, zero_opt_step_info* out) {
+  if (!h || !out) return fail(ZERO_EINVAL, "NULL argument");
+  std::memcpy(out, &h->last, sizeof(*out));
+  return ZERO_OK;
+}
+
+}  // extern "C"

@@ -31,6 +31,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "decide_core.h"
 #include "zero_opt_internal.h"
 
 // Resident CTAs per SM each kernel is compiled for (register budget 65536 /
@@ -40,6 +41,11 @@
 #endif
 #ifndef ZO_PASS2_MIN_CTAS
 #define ZO_PASS2_MIN_CTAS 2
+#endif
+// The multi-buffer pass 1 holds eight 16-byte loads in flight per thread and
+// needs the larger register budget of three CTAs per SM.
+#ifndef ZO_MULTI_MIN_CTAS
+#define ZO_MULTI_MIN_CTAS 3
 #endif
 // Tiles whose 16-byte gradient loads pass 1 issues before reducing any of
 // them, when there is a single gradient buffer.
@@ -195,8 +201,47 @@ __device__ __forceinline__ const unsigned short* grad_ptr(const void* const* gpt
 // or whose values are all nonzero and below 2^-40 (squares near underflow),
 // are summed in binary64 instead.  amax (the largest |s| bit pattern seen)
 // gives the overflow flag: inf and NaN patterns are >= 0x7f800000.
+#ifndef ZO_PACKED_SQ
+#define ZO_PACKED_SQ 1
+#endif
+
+// Two binary32 lanes in one 64-bit register, for the f32x2 instructions.  The
+// explicit .rn rounding keeps each lane an IEEE binary32 operation that the
+// compiler never contracts, so a lane rounds exactly as the scalar _rn
+// intrinsic does.
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 f2_pack(float a, float b) {
+  return (f32x2)__float_as_uint(a) | ((f32x2)__float_as_uint(b) << 32);
+}
+__device__ __forceinline__ float f2_lo(f32x2 v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float f2_hi(f32x2 v) { return __uint_as_float((uint32_t)(v >> 32)); }
+__device__ __forceinline__ f32x2 f2_add(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 f2_sub(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 f2_mul(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 struct SqAcc {
+#if ZO_PACKED_SQ
+  f32x2 H = 0ull, L = 0ull;  // lane 0 and lane 1 in one register each
+#else
   float hi0 = 0.0f, lo0 = 0.0f, hi1 = 0.0f, lo1 = 0.0f;
+#endif
   double slow = 0.0;
   uint32_t amax = 0u;
 
@@ -222,6 +267,37 @@ struct SqAcc {
     hi = t;
   }
 
+  // a to lane 0, b to lane 1.
+  __device__ __forceinline__ void pair(float a, float b) {
+#if ZO_PACKED_SQ
+    const f32x2 X = f2_pack(a, b);
+    const f32x2 P = f2_mul(X, X);
+    const f32x2 E = f2_fma(X, X, P ^ 0x8000000080000000ull);
+    const f32x2 T = f2_add(H, P);
+    const f32x2 BP = f2_sub(T, H);
+    const f32x2 AP = f2_sub(T, BP);
+    L = f2_add(L, f2_add(f2_add(f2_sub(H, AP), f2_sub(P, BP)), E));
+    H = T;
+#else
+    two_sum_add(hi0, lo0, a);
+    two_sum_add(hi1, lo1, b);
+#endif
+  }
+  __device__ __forceinline__ void pair_exact(float a, float b) {
+#if ZO_PACKED_SQ
+    const f32x2 X = f2_pack(a, b);
+    const f32x2 P = f2_mul(X, X);
+    const f32x2 T = f2_add(H, P);
+    const f32x2 BP = f2_sub(T, H);
+    const f32x2 AP = f2_sub(T, BP);
+    L = f2_add(L, f2_add(f2_sub(H, AP), f2_sub(P, BP)));
+    H = T;
+#else
+    two_sum_add_exact(hi0, lo0, a);
+    two_sum_add_exact(hi1, lo1, b);
+#endif
+  }
+
   // EXACT_SQ: every s is a converted 16-bit value, whose square (fp16: 22
   // significant bits, bf16: 16) is exact in binary32 inside the fast range.
   template <bool EXACT_SQ = false>
@@ -234,13 +310,8 @@ struct SqAcc {
     if (fast) {
 #pragma unroll
       for (int i = 0; i < kVec; i += 2) {
-        if (EXACT_SQ) {
-          two_sum_add_exact(hi0, lo0, s[i]);
-          two_sum_add_exact(hi1, lo1, s[i + 1]);
-        } else {
-          two_sum_add(hi0, lo0, s[i]);
-          two_sum_add(hi1, lo1, s[i + 1]);
-        }
+        if (EXACT_SQ) pair_exact(s[i], s[i + 1]);
+        else pair(s[i], s[i + 1]);
       }
     } else {
       double d = 0.0;
@@ -265,8 +336,7 @@ struct SqAcc {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const float2 x = Fmt<GT>::dec2(w[k]);
-        two_sum_add_exact(hi0, lo0, x.x);
-        two_sum_add_exact(hi1, lo1, x.y);
+        pair_exact(x.x, x.y);
       }
     } else {
       double d = 0.0;
@@ -285,6 +355,9 @@ struct SqAcc {
   }
 
   __device__ __forceinline__ double total() const {
+#if ZO_PACKED_SQ
+    const float hi0 = f2_lo(H), lo0 = f2_lo(L), hi1 = f2_hi(H), lo1 = f2_hi(L);
+#endif
     const double a = __dadd_rn((double)hi0, (double)lo0);
     const double b = __dadd_rn((double)hi1, (double)lo1);
     return __dadd_rn(__dadd_rn(a, b), slow);
@@ -308,108 +381,57 @@ __device__ __forceinline__ double block_sum(double x, double* red) {
 }
 
 // ------------------------------------------------------------- decisions (a4)
-// Run by one thread of the last CTA.  Scalars are computed in binary64 and
-// rounded once to binary32.  Overflow: skip, clean count restarts, and on the
-// hysteresis-th overflow since the scale last changed scale /= factor (not
-// below min_scale).  The update's lr is lr, or WarmupLR's linear value.  Otherwise: norm of the unscaled gradient,
-// clip coefficient min(1, max_norm / (norm + 1e-6)), Adam step t += 1 with its
-// bias corrections, and the scale grows by the factor after `window`
-// consecutive applied steps.
-static __device__ void decide(const Pass1Args& a, double own_sumsq, int own_flag) {
+// The decision itself is decide_core (decide_core.h); here are the device
+// parts around it: the scalar CTA's early computation of the next step's
+// update scalars, and the last CTA's call with the folded statistics.
+
+// Run by thread 0 of pass 1's scalar CTA while the other CTAs stream: the
+// scalars of the step that follows the current one (t + 1; the step counter
+// only changes in the decision at the end of this launch), so that the
+// decision, which waits for every CTA, does no binary64 pow.
+static __device__ __noinline__ void precompute_scalars(const Pass1Args& a) {
+  PreScalars p;
+  p.t = a.ranks[a.rank].t + 1;
+  step_scalars(a.hp, p.t, &p.step_size, &p.isb2, &p.decay);
+  p.pad_ = 0;
+  a.ws->pre = p;
+}
+
+// True for the CTA that streams nothing (the last one, when scalar_cta is set).
+__device__ __forceinline__ bool is_scalar_cta(const Pass1Args& a) {
+  return a.scalar_cta && blockIdx.x == gridDim.x - 1;
+}
+
+// Run by one thread of the last CTA of pass 1.  A statistics-only pass just
+// publishes its statistics (after a fault: an overflow, so that every rank
+// that folds them skips).  A fault skips the step and leaves the scaler state
+// alone.  Otherwise the rank's scaler replica advances through decide_core.
+static __device__ __noinline__ void decide(const Pass1Args& a, double own_sumsq, int own_flag) {
   Workspace* ws = a.ws;
   ws->ticket = 0u;
   const int fault = ws->fault;
   ws->fault = 0;
   if (a.mode == kStatsOnly) {
-    // after a fault the statistics are incomplete: report an overflow so that
-    // every rank that folds them skips the step
-    ws->own_sumsq = fault ? __longlong_as_double(0x7ff8000000000000ll) : own_sumsq;
+    ws->own_sumsq = fault ? quiet_nan() : own_sumsq;
     ws->own_nonfinite = fault ? 1 : own_flag;
     return;
   }
   if (fault) {
-    // a bounded wait expired: skip without touching the scaler state
-    Decision d;
-    d.sumsq = d.norm = __longlong_as_double(0x7ff8000000000000ll);
-    d.coef = d.scale_used = 0.0f;
-    d.skip = 1;
-    d.nonfinite = 0;
-    d.t = a.ranks[a.rank].t;
-    d.fault = 1;
-    d.pad_ = 0;
-    d.step_size = d.isb2 = d.decay = d.b1 = d.omb1 = d.b2 = d.omb2 = d.eps = 0.0f;
-    d.scale_used = a.ranks[a.rank].scale;
-    ws->dec = d;
+    ws->dec = fault_decision(a.ranks[a.rank]);
     return;
   }
   const double sumsq = a.mode == kStepGlobal ? a.g_sumsq : own_sumsq;
   const int nonfinite = a.mode == kStepGlobal ? a.g_nonfinite : own_flag;
   RankState st = a.ranks[a.rank];
-  Decision d;
-  d.fault = 0;
-  d.pad_ = 0;
-  d.sumsq = sumsq;
-  d.nonfinite = nonfinite;
-  d.scale_used = st.scale;
-  d.coef = 0.0f;
-  d.step_size = d.isb2 = d.decay = d.b1 = d.omb1 = d.b2 = d.omb2 = d.eps = 0.0f;
-  const float scale = st.scale;
-  const double inv = 1.0 / ((double)scale * a.hp.divisor);
-  if (nonfinite) {
-    d.skip = 1;
-    d.norm = __longlong_as_double(0x7ff8000000000000ll);
-    if (a.hp.dynamic) {
-      st.overflows += 1;
-      if (st.overflows >= a.hp.hysteresis) {
-        double lowered = (double)scale / a.hp.factor;
-        if (lowered < a.hp.min_scale) lowered = a.hp.min_scale;
-        st.scale = (float)lowered;
-        st.overflows = 0;
-      }
-    }
-    st.clean = 0;
-    st.skipped_total += 1;
-    st.last_skipped = 1;
-  } else {
-    const double norm = sqrt(sumsq) * inv;
-    double clip = 1.0;
-    if (a.hp.max_norm > 0.0) {
-      clip = a.hp.max_norm / (norm + 1e-6);
-      if (clip > 1.0) clip = 1.0;
-    }
-    d.skip = 0;
-    d.norm = norm;
-    d.coef = (float)(inv * clip);
-    st.t += 1;
-    double bc1 = 1.0, bc2 = 1.0;
-    if (a.hp.bias_correction) {
-      bc1 = 1.0 - pow(a.hp.beta1, (double)st.t);
-      bc2 = 1.0 - pow(a.hp.beta2, (double)st.t);
-    }
-    double lr = a.hp.lr;
-    if (a.hp.warmup_num_steps > 0) {
-      const double T = (double)a.hp.warmup_num_steps;
-      const double t = (double)st.t;
-      const double frac = t < T ? t / T : 1.0;
-      lr = a.hp.warmup_min_lr + (a.hp.warmup_max_lr - a.hp.warmup_min_lr) * frac;
-    }
-    d.step_size = (float)(lr / bc1);
-    d.isb2 = (float)(1.0 / sqrt(bc2));
-    d.decay = (float)(1.0 - lr * a.hp.wd);
-    d.b1 = (float)a.hp.beta1;
-    d.omb1 = (float)(1.0 - a.hp.beta1);
-    d.b2 = (float)a.hp.beta2;
-    d.omb2 = (float)(1.0 - a.hp.beta2);
-    d.eps = (float)a.hp.eps;
-    st.last_skipped = 0;
-    st.clean += 1;
-    if (a.hp.dynamic && st.clean == a.hp.window) {
-      st.scale = (float)((double)scale * a.hp.factor);
-      st.clean = 0;
-      st.overflows = 0;
-    }
-  }
-  d.t = st.t;
+  // every stepping launch has a scalar CTA, which stored the scalars of step
+  // t + 1 before this CTA could take the last ticket
+  const volatile PreScalars* pre = &ws->pre;
+  const Decision d = decide_core(a.hp, st, sumsq, nonfinite,
+                                 [pre](int64_t, float* ss, float* isb2, float* decay) {
+                                   *ss = pre->step_size;
+                                   *isb2 = pre->isb2;
+                                   *decay = pre->decay;
+                                 });
   a.ranks[a.rank] = st;
   ws->dec = d;
 }
@@ -446,15 +468,20 @@ __device__ __forceinline__ void pass1_finish(const Pass1Args& a, double mine, in
 
 // One tile element by element: a ragged tail of a vector run (e >= e0 within
 // the thread's 8 elements) or any tile of a run with a misaligned pointer
-// (elements base + i*256 + tid, coalesced).  Kept out of line: it is rare, and
-// inlining it would cost the main loops registers.
+// (elements base + i*256 + tid, coalesced).  Returns the thread's 8 sums (0
+// past the end) by value, so that callers keep their accumulators in
+// registers; kept out of line because it is rare.
+struct Sums8 {
+  float v[kVec];
+};
+
 template <typename GT, bool STASH>
-__device__ __noinline__ void pass1_elementwise_tile(const Pass1Args& a, int64_t n,
-                                                    int64_t stash_off, int32_t gbase,
-                                                    int32_t vec, int64_t base, SqAcc& acc) {
+__device__ __noinline__ Sums8 pass1_elementwise_sums(const Pass1Args& a, int64_t n,
+                                                     int64_t stash_off, int32_t gbase,
+                                                     int32_t vec, int64_t base) {
   const int tid = threadIdx.x;
   const int64_t e0 = base + tid * kVec;
-  float x[kVec];
+  Sums8 x;
 #pragma unroll
   for (int i = 0; i < kVec; ++i) {
     const int64_t e = vec ? e0 + i : base + (int64_t)i * kThreads + tid;
@@ -467,9 +494,9 @@ __device__ __noinline__ void pass1_elementwise_tile(const Pass1Args& a, int64_t 
       }
       if (STASH) a.stash[stash_off + e] = sum;
     }
-    x[i] = sum;
+    x.v[i] = sum;
   }
-  acc.add<false>(x);
+  return x;
 }
 
 // Single gradient buffer (R*K = 1, never stashed).  ZO_PASS1_UNROLL tiles'
@@ -482,10 +509,11 @@ __global__ void __launch_bounds__(kThreads, ZO_PASS1_MIN_CTAS)
   __shared__ int s_last;
   constexpr int U = ZO_PASS1_UNROLL;
   const int tid = threadIdx.x;
-  const int64_t G = gridDim.x;
+  const int64_t G = gridDim.x - a.scalar_cta;
+  if (is_scalar_cta(a) && tid == 0) precompute_scalars(a);
   SqAcc acc;
   RunCursorLite cur;
-  for (int64_t t0 = blockIdx.x; t0 < a.ntiles; t0 += U * G) {
+  for (int64_t t0 = blockIdx.x; t0 < a.ntiles && blockIdx.x < G; t0 += U * G) {
     uint4 raw[U];
     bool fast[U];
 #pragma unroll
@@ -511,8 +539,9 @@ __global__ void __launch_bounds__(kThreads, ZO_PASS1_MIN_CTAS)
         acc.add_raw16<GT>(raw[u]);
       } else {
         cur.seek(a.segs, a.nseg, tile);
-        pass1_elementwise_tile<GT, false>(a, cur.s.n, cur.s.stash_off, cur.s.gbase, cur.s.vec,
-                                          (tile - cur.s.tile0) * kTile, acc);
+        const Sums8 x = pass1_elementwise_sums<GT, false>(a, cur.s.n, cur.s.stash_off, cur.s.gbase,
+                                                          cur.s.vec, (tile - cur.s.tile0) * kTile);
+        acc.add<false>(x.v);
       }
     }
   }
@@ -578,40 +607,58 @@ __device__ __forceinline__ bool mbar_wait_bounded(unsigned long long* bar, uint3
 }
 
 #ifndef ZO_BULK_STAGES
-#define ZO_BULK_STAGES 8
+#define ZO_BULK_STAGES 2
 #endif
 
-// Single gradient buffer, staged through shared memory by bulk copies: thread
-// 0 keeps ZO_BULK_STAGES tiles (4 KiB each for 16-bit gradients) in flight per
-// CTA, so the reducing threads never wait on global memory.  A tile that is
-// not a full 16-byte aligned tile (a run's ragged tail, a misaligned run) is
-// not copied: its barrier phase is completed by a plain arrival and the tile
-// is reduced element by element from global memory.  If a wait expires the
-// CTA stops issuing copies, waits (again bounded) for those in flight, and
+// Bytes of dynamic shared memory pass1_bulk_kernel<GT, CT> needs.
+constexpr int bulk_smem_bytes(int chunk_tiles) {
+  return ZO_BULK_STAGES * chunk_tiles * kThreads * 16;
+}
+// Resident CTAs per SM each chunk size is compiled for.
+constexpr int bulk_min_ctas(int chunk_tiles) { return chunk_tiles >= 8 ? 3 : ZO_PASS1_MIN_CTAS; }
+
+// Single gradient buffer, staged through shared memory by bulk copies.  The
+// work unit is a chunk of CT consecutive tiles (each thread reduces 8*CT
+// elements per chunk); thread 0 keeps ZO_BULK_STAGES chunks in flight per CTA
+// with one cp.async.bulk of CT * 4 KiB each, so the reducing threads read
+// shared memory instead of waiting on global loads.  Chunks of 4 tiles at 4
+// CTAs per SM balance short shards best; chunks of 8 tiles at 3 CTAs per SM
+// move more per copy on long ones.  A chunk that is not CT full tiles of one
+// 16-byte aligned run is not copied: its barrier phase is completed by a
+// plain arrival and its tiles are reduced from global memory.  If a wait
+// expires the CTA stops issuing, waits (bounded) for the copies in flight and
 // records a fault, which makes the step a no-op.
-template <typename GT>
-__global__ void __launch_bounds__(kThreads, ZO_PASS1_MIN_CTAS)
+template <typename GT, int CT>
+__global__ void __launch_bounds__(kThreads, bulk_min_ctas(CT))
     pass1_bulk_kernel(const Pass1Args a) {
   constexpr int S = ZO_BULK_STAGES;
-  __shared__ __align__(128) uint4 buf[S][kThreads];
+  constexpr int kChunkTiles = CT;
+  extern __shared__ __align__(128) uint4 stage_buf[];  // [S][CT][kThreads]
   __shared__ __align__(8) unsigned long long bar[S];
   __shared__ double red[kThreads / 32];
   __shared__ int s_last, s_err;
   const int tid = threadIdx.x;
-  const int64_t G = gridDim.x;
-  const int64_t mine = (a.ntiles > (int64_t)blockIdx.x)
-                           ? (a.ntiles - 1 - (int64_t)blockIdx.x) / G + 1
+  const int64_t G = gridDim.x - a.scalar_cta;
+  const int64_t nchunks = (a.ntiles + kChunkTiles - 1) / kChunkTiles;
+  const int64_t mine = (int64_t)blockIdx.x < G && nchunks > (int64_t)blockIdx.x
+                           ? (nchunks - 1 - blockIdx.x) / G + 1
                            : 0;
+  // a chunk is copied whole when its four tiles are full tiles of one vector run
+  auto whole = [&](RunCursorLite& c, int64_t t0) -> bool {
+    c.seek(a.segs, a.nseg, t0);
+    return c.s.vec && t0 + kChunkTiles <= c.end &&
+           (t0 + kChunkTiles - c.s.tile0) * kTile <= c.s.n;
+  };
   RunCursorLite pcur;  // thread 0's cursor for issuing copies
   auto issue = [&](int64_t i) {
-    const int64_t tile = blockIdx.x + i * G;
+    const int64_t t0 = (blockIdx.x + i * G) * kChunkTiles;
     unsigned long long* b = &bar[i % S];
-    if (a.inject_wait_fault && blockIdx.x == 0 && i == 1) return;  // test hook
-    pcur.seek(a.segs, a.nseg, tile);
-    const int64_t base = (tile - pcur.s.tile0) * kTile;
-    if (pcur.s.vec && base + kTile <= pcur.s.n) {
-      mbar_arrive_expect_tx(b, kTile * 2);
-      bulk_load(&buf[i % S][0], grad_ptr(a.gptrs, pcur.s, 0) + base, kTile * 2, b);
+    if (a.inject_wait_fault && blockIdx.x == 0 && i == 0) return;  // test hook
+    if (whole(pcur, t0)) {
+      mbar_arrive_expect_tx(b, kChunkTiles * kTile * 2);
+      bulk_load(&stage_buf[(i % S) * kChunkTiles * kThreads],
+                grad_ptr(a.gptrs, pcur.s, 0) + (t0 - pcur.s.tile0) * kTile,
+                kChunkTiles * kTile * 2, b);
     } else {
       mbar_arrive(b);
     }
@@ -620,6 +667,7 @@ __global__ void __launch_bounds__(kThreads, ZO_PASS1_MIN_CTAS)
     for (int k = 0; k < S; ++k) mbar_init(&bar[k], 1);
     mbar_init_fence();
     s_err = 0;
+    if (is_scalar_cta(a)) precompute_scalars(a);
   }
   __syncthreads();
   if (tid == 0)
@@ -628,21 +676,33 @@ __global__ void __launch_bounds__(kThreads, ZO_PASS1_MIN_CTAS)
   RunCursorLite cur;
   int64_t issued = mine < S ? mine : S;
   for (int64_t i = 0; i < mine; ++i) {
-    const uint32_t parity = (uint32_t)((i / S) & 1);
-    if (!mbar_wait_bounded(&bar[i % S], parity)) s_err = 1;
-    const int64_t tile = blockIdx.x + i * G;
-    cur.seek(a.segs, a.nseg, tile);
-    const int64_t base = (tile - cur.s.tile0) * kTile;
+    if (!mbar_wait_bounded(&bar[i % S], (uint32_t)((i / S) & 1))) s_err = 1;
+    const int64_t t0 = (blockIdx.x + i * G) * kChunkTiles;
     if (!s_err) {
-      if (cur.s.vec && base + kTile <= cur.s.n)
-        acc.add_raw16<GT>(buf[i % S][tid]);
-      else
-        pass1_elementwise_tile<GT, false>(a, cur.s.n, cur.s.stash_off, cur.s.gbase, cur.s.vec,
-                                          base, acc);
+      if (whole(cur, t0)) {
+        const uint4* sb = &stage_buf[(i % S) * kChunkTiles * kThreads + tid];
+#pragma unroll
+        for (int k = 0; k < kChunkTiles; ++k) acc.add_raw16<GT>(sb[k * kThreads]);
+      } else {
+        for (int k = 0; k < kChunkTiles; ++k) {
+          const int64_t tile = t0 + k;
+          if (tile >= a.ntiles) break;
+          cur.seek(a.segs, a.nseg, tile);
+          const int64_t base = (tile - cur.s.tile0) * kTile;
+          if (cur.s.vec && base + kTile <= cur.s.n) {
+            acc.add_raw16<GT>(__ldcg(reinterpret_cast<const uint4*>(
+                grad_ptr(a.gptrs, cur.s, 0) + base + tid * kVec)));
+          } else {
+            const Sums8 x = pass1_elementwise_sums<GT, false>(a, cur.s.n, cur.s.stash_off,
+                                                              cur.s.gbase, cur.s.vec, base);
+            acc.add<false>(x.v);
+          }
+        }
+      }
     }
     __syncthreads();  // every thread is done with stage i % S
     if (s_err) {
-      // drain the copies still in flight before the CTA's shared memory goes
+      // wait for the copies still in flight before the shared memory goes away
       if (tid == 0) {
         for (int64_t j = i; j < issued; ++j)
           (void)mbar_wait_bounded(&bar[j % S], (uint32_t)((j / S) & 1));
@@ -661,20 +721,23 @@ __global__ void __launch_bounds__(kThreads, ZO_PASS1_MIN_CTAS)
 // Any number of gradient buffers, loaded in batches of eight per tile, summed
 // in buffer order; optionally stores the sums (the stash).
 template <typename GT, bool STASH>
-__global__ void __launch_bounds__(kThreads, ZO_PASS1_MIN_CTAS)
+__global__ void __launch_bounds__(kThreads, ZO_MULTI_MIN_CTAS)
     pass1_multi_kernel(const Pass1Args a) {
   __shared__ double red[kThreads / 32];
   __shared__ int s_last;
   const int tid = threadIdx.x;
+  const int64_t G = gridDim.x - a.scalar_cta;
+  if (is_scalar_cta(a) && tid == 0) precompute_scalars(a);
   SqAcc acc;
   RunCursorLite cur;
-  for (int64_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
+  for (int64_t tile = blockIdx.x; tile < a.ntiles && blockIdx.x < G; tile += G) {
     cur.seek(a.segs, a.nseg, tile);
     const auto& s = cur.s;
     const int64_t base = (tile - s.tile0) * kTile;
     const int64_t e0 = base + tid * kVec;
     if (!(s.vec && e0 + kVec <= s.n)) {
-      pass1_elementwise_tile<GT, STASH>(a, s.n, s.stash_off, s.gbase, s.vec, base, acc);
+      const Sums8 x = pass1_elementwise_sums<GT, STASH>(a, s.n, s.stash_off, s.gbase, s.vec, base);
+      acc.add<false>(x.v);
       continue;
     }
     float x[kVec];

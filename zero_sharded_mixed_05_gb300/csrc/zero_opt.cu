@@ -55,6 +55,55 @@ void shard_range(int64_t numel, int32_t world, int32_t rank, int64_t* begin,
   *shard_len = S;
 }
 
+// Validation of a configuration shared by the device and host handles.
+zero_status check_config(const zero_opt_config* c) {
+  if (c->numel < 0) return fail(ZERO_EINVAL, "numel must be >= 0");
+  if (c->world < 1) return fail(ZERO_EINVAL, "world must be >= 1");
+  if ((c->grad_dtype != ZERO_FP16 && c->grad_dtype != ZERO_BF16) ||
+      (c->param_dtype != ZERO_FP16 && c->param_dtype != ZERO_BF16))
+    return fail(ZERO_EINVAL, "dtype must be ZERO_FP16 or ZERO_BF16");
+  if (!(c->lr >= 0.0)) return fail(ZERO_EINVAL, "lr must be >= 0");
+  if (!(c->beta1 >= 0.0 && c->beta1 < 1.0) || !(c->beta2 >= 0.0 && c->beta2 < 1.0))
+    return fail(ZERO_EINVAL, "betas must lie in [0, 1)");
+  if (!(c->eps > 0.0)) return fail(ZERO_EINVAL, "eps must be > 0");
+  if (!(c->weight_decay >= 0.0)) return fail(ZERO_EINVAL, "weight_decay must be >= 0");
+  if (std::isnan(c->max_grad_norm)) return fail(ZERO_EINVAL, "max_grad_norm is NaN");
+  if (!(c->init_scale > 0.0) || !(c->min_scale > 0.0))
+    return fail(ZERO_EINVAL, "init_scale and min_scale must be > 0");
+  if (!(c->scale_factor >= 1.0)) return fail(ZERO_EINVAL, "scale_factor must be >= 1");
+  if (c->scale_window < 1) return fail(ZERO_EINVAL, "scale_window must be >= 1");
+  if (c->bias_correction != 0 && c->bias_correction != 1)
+    return fail(ZERO_EINVAL, "bias_correction must be 0 or 1");
+  if (c->dynamic_scale != 0 && c->dynamic_scale != 1)
+    return fail(ZERO_EINVAL, "dynamic_scale must be 0 or 1");
+  if (c->hysteresis < 1) return fail(ZERO_EINVAL, "hysteresis must be >= 1");
+  if (c->warmup_num_steps < 0 || !(c->warmup_min_lr >= 0.0) || !(c->warmup_max_lr >= 0.0))
+    return fail(ZERO_EINVAL, "warm-up steps and learning rates must be >= 0");
+  return ZERO_OK;
+}
+
+// Kernel-side hyperparameters of a configuration, in binary64.
+Hyper hyper_of(const zero_opt_config& c, double divisor) {
+  Hyper hp;
+  hp.lr = c.lr;
+  hp.beta1 = c.beta1;
+  hp.beta2 = c.beta2;
+  hp.eps = c.eps;
+  hp.wd = c.weight_decay;
+  hp.max_norm = c.max_grad_norm;
+  hp.divisor = divisor;
+  hp.min_scale = c.min_scale;
+  hp.factor = c.scale_factor;
+  hp.window = c.scale_window;
+  hp.bias_correction = c.bias_correction;
+  hp.dynamic = c.dynamic_scale;
+  hp.hysteresis = c.hysteresis;
+  hp.warmup_min_lr = c.warmup_min_lr;
+  hp.warmup_max_lr = c.warmup_max_lr;
+  hp.warmup_num_steps = c.warmup_num_steps;
+  return hp;
+}
+
 }  // namespace zo
 
 namespace {
@@ -112,32 +161,6 @@ namespace {
 
 constexpr size_t kPinnedBytes = 256;
 
-zero_status check_config(const zero_opt_config* c) {
-  if (c->numel < 0) return fail(ZERO_EINVAL, "numel must be >= 0");
-  if (c->world < 1) return fail(ZERO_EINVAL, "world must be >= 1");
-  if ((c->grad_dtype != ZERO_FP16 && c->grad_dtype != ZERO_BF16) ||
-      (c->param_dtype != ZERO_FP16 && c->param_dtype != ZERO_BF16))
-    return fail(ZERO_EINVAL, "dtype must be ZERO_FP16 or ZERO_BF16");
-  if (!(c->lr >= 0.0)) return fail(ZERO_EINVAL, "lr must be >= 0");
-  if (!(c->beta1 >= 0.0 && c->beta1 < 1.0) || !(c->beta2 >= 0.0 && c->beta2 < 1.0))
-    return fail(ZERO_EINVAL, "betas must lie in [0, 1)");
-  if (!(c->eps > 0.0)) return fail(ZERO_EINVAL, "eps must be > 0");
-  if (!(c->weight_decay >= 0.0)) return fail(ZERO_EINVAL, "weight_decay must be >= 0");
-  if (std::isnan(c->max_grad_norm)) return fail(ZERO_EINVAL, "max_grad_norm is NaN");
-  if (!(c->init_scale > 0.0) || !(c->min_scale > 0.0))
-    return fail(ZERO_EINVAL, "init_scale and min_scale must be > 0");
-  if (!(c->scale_factor >= 1.0)) return fail(ZERO_EINVAL, "scale_factor must be >= 1");
-  if (c->scale_window < 1) return fail(ZERO_EINVAL, "scale_window must be >= 1");
-  if (c->bias_correction != 0 && c->bias_correction != 1)
-    return fail(ZERO_EINVAL, "bias_correction must be 0 or 1");
-  if (c->dynamic_scale != 0 && c->dynamic_scale != 1)
-    return fail(ZERO_EINVAL, "dynamic_scale must be 0 or 1");
-  if (c->hysteresis < 1) return fail(ZERO_EINVAL, "hysteresis must be >= 1");
-  if (c->warmup_num_steps < 0 || !(c->warmup_min_lr >= 0.0) || !(c->warmup_max_lr >= 0.0))
-    return fail(ZERO_EINVAL, "warm-up steps and learning rates must be >= 0");
-  return ZERO_OK;
-}
-
 void shard_of(const zero_opt_config& c, int rank, int64_t* begin, int64_t* real_end,
               int64_t* shard, int64_t* padded) {
   const int64_t S = (c.numel + c.world - 1) / c.world;
@@ -167,11 +190,28 @@ zero_status check_device(zero_opt_t h) {
   return ZERO_OK;
 }
 
+// Dynamic shared memory a kernel is launched with (the bulk-copy pass 1 stages
+// its chunks there; everything else uses none).
+size_t dyn_smem(const void* fn) {
+  if (fn == reinterpret_cast<const void*>(zo::pass1_bulk_kernel<__half, 4>) ||
+      fn == reinterpret_cast<const void*>(zo::pass1_bulk_kernel<__nv_bfloat16, 4>))
+    return zo::bulk_smem_bytes(4);
+  if (fn == reinterpret_cast<const void*>(zo::pass1_bulk_kernel<__half, 8>) ||
+      fn == reinterpret_cast<const void*>(zo::pass1_bulk_kernel<__nv_bfloat16, 8>))
+    return zo::bulk_smem_bytes(8);
+  return 0;
+}
+
 int occupancy(zero_opt_t h, const void* fn) {
   for (auto& kv : h->occ)
     if (kv.first == fn) return kv.second;
+  // the opt-in limit counts static + dynamic shared memory against 48 KiB, so
+  // it is raised for every kernel that takes dynamic shared memory
+  const size_t smem = dyn_smem(fn);
+  if (smem > 0)
+    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, zo::kThreads, 0) != cudaSuccess ||
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, zo::kThreads, smem) != cudaSuccess ||
       n < 1)
     n = 1;
   h->occ.emplace_back(fn, n);
@@ -264,11 +304,22 @@ zero_status get_plan(zero_opt_t h, const std::vector<HostRun>& runs, int nbuf,
 using Pass1Fn = void (*)(zo::Pass1Args);
 using Pass2Fn = void (*)(zo::Pass2Args);
 
-Pass1Fn pick_pass1(int gdt, bool stash, bool one) {
+// Tiles from which a single-buffer shard takes 8-tile bulk chunks (about 410M
+// elements: at least ~60 chunks per CTA, so the coarser unit costs little
+// balance).
+constexpr int64_t kBigChunkTiles = 200000;
+
+Pass1Fn pick_pass1(int gdt, bool stash, bool one, int64_t ntiles) {
   // a single buffer is never stashed (the stash needs more than four)
 #if ZO_PASS1_BULK
-  if (one) return gdt == ZERO_FP16 ? zo::pass1_bulk_kernel<__half>
-                                   : zo::pass1_bulk_kernel<__nv_bfloat16>;
+  if (one) {
+    const bool big = ntiles >= kBigChunkTiles;
+    if (gdt == ZERO_FP16)
+      return big ? zo::pass1_bulk_kernel<__half, 8> : zo::pass1_bulk_kernel<__half, 4>;
+    return big ? zo::pass1_bulk_kernel<__nv_bfloat16, 8> : zo::pass1_bulk_kernel<__nv_bfloat16, 4>;
+  }
+#else
+  (void)ntiles;
 #endif
   if (gdt == ZERO_FP16) {
     if (one) return zo::pass1_single_kernel<__half>;
@@ -294,31 +345,12 @@ Pass2Fn pick_pass2(int gdt, int pdt, int src) {
                           : pick_pass2_t<__nv_bfloat16, __nv_bfloat16>(src);
 }
 
-zo::Hyper hyper_of(const zero_opt_config& c, double divisor) {
-  zo::Hyper hp;
-  hp.lr = c.lr;
-  hp.beta1 = c.beta1;
-  hp.beta2 = c.beta2;
-  hp.eps = c.eps;
-  hp.wd = c.weight_decay;
-  hp.max_norm = c.max_grad_norm;
-  hp.divisor = divisor;
-  hp.min_scale = c.min_scale;
-  hp.factor = c.scale_factor;
-  hp.window = c.scale_window;
-  hp.bias_correction = c.bias_correction;
-  hp.dynamic = c.dynamic_scale;
-  hp.hysteresis = c.hysteresis;
-  hp.warmup_min_lr = c.warmup_min_lr;
-  hp.warmup_max_lr = c.warmup_max_lr;
-  hp.warmup_num_steps = c.warmup_num_steps;
-  return hp;
-}
 
 zero_status launch_kernel(zero_opt_t h, const void* fn, int grid, void* args,
                           cudaStream_t stream) {
   void* params[] = {args};
-  cudaError_t e = cudaLaunchKernel(fn, dim3(grid), dim3(zo::kThreads), params, 0, stream);
+  cudaError_t e = cudaLaunchKernel(fn, dim3(grid), dim3(zo::kThreads), params, dyn_smem(fn),
+                                   stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernel");
   h->launches += 1;
   return ZERO_OK;
@@ -356,17 +388,22 @@ zero_status run(zero_opt_t h, int32_t rank, const std::vector<HostRun>& runs, in
     a1.g_sumsq = global->sumsq;
     a1.g_nonfinite = global->nonfinite ? 1 : 0;
   }
-  a1.hp = hyper_of(h->cfg, divisor);
+  a1.hp = zo::hyper_of(h->cfg, divisor);
   a1.ws = h->ws;
   a1.ranks = h->ranks;
   a1.inject_wait_fault = h->inject_wait_fault;
   h->inject_wait_fault = 0;
 
   const void* f1 = reinterpret_cast<const void*>(
-      pick_pass1(h->cfg.grad_dtype, use_stash != nullptr, nbuf == 1));
-  int64_t g1 = (int64_t)occupancy(h, f1) * h->sms;
+      pick_pass1(h->cfg.grad_dtype, use_stash != nullptr, nbuf == 1, plan->ntiles));
+  // Every step launch gets one extra CTA that computes the next step's update
+  // scalars (binary64 pow) while the others stream, so the decision at the
+  // end of the launch does none; it takes one of the resident slots so that
+  // every CTA runs at once.
+  a1.scalar_cta = mode != zo::kStatsOnly ? 1 : 0;
+  int64_t g1 = (int64_t)occupancy(h, f1) * h->sms - a1.scalar_cta;
   g1 = std::min<int64_t>(g1, std::max<int64_t>(a1.ntiles, 1));
-  g1 = std::min<int64_t>(g1, zo::kMaxCtas);
+  g1 = std::max<int64_t>(std::min<int64_t>(g1, zo::kMaxCtas - 1), 1) + a1.scalar_cta;
   if (h->ev[0]) cudaEventRecord(h->ev[0], stream);
   st = launch_kernel(h, f1, (int)g1, &a1, stream);
   if (h->ev[1]) cudaEventRecord(h->ev[1], stream);
@@ -521,7 +558,7 @@ zero_status zero_opt_create(const zero_opt_config* cfg, zero_opt_t* out) {
   if (!out) return fail(ZERO_EINVAL, "out is NULL");
   *out = nullptr;
   if (!cfg) return fail(ZERO_EINVAL, "cfg is NULL");
-  zero_status st = check_config(cfg);
+  zero_status st = zo::check_config(cfg);
   if (st != ZERO_OK) return st;
   zero_opt_handle* h = new (std::nothrow) zero_opt_handle;
   if (!h) return fail(ZERO_ENOMEM, "handle allocation failed");

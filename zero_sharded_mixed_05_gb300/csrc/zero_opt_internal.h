@@ -58,10 +58,19 @@ struct Decision {
 };
 static_assert(sizeof(zero_opt_step_info) <= sizeof(Decision), "layout");
 
+// The step-dependent update scalars for Adam step t, computed ahead of the
+// decision by pass 1's scalar CTA.
+struct PreScalars {
+  int64_t t;             // the step they belong to; 0: none
+  float step_size, isb2, decay;
+  int32_t pad_;
+};
+
 struct Workspace {
   unsigned int ticket;   // CTAs of pass 1 that finished; reset by the last
   int32_t fault;         // set by a CTA whose bounded wait expired; reset by decide
   Decision dec;          // written by the last CTA of pass 1, read by pass 2
+  PreScalars pre;        // written by the scalar CTA, read by decide
   double own_sumsq;      // statistics-only result
   int32_t own_nonfinite;
   int32_t pad1;
@@ -96,7 +105,8 @@ struct Pass1Args {
   Workspace* ws;
   RankState* ranks;
   int32_t inject_wait_fault;   // test hook: leave one bulk-copy barrier un-armed
-  int32_t pad2;
+  int32_t scalar_cta;          // 1: the last CTA streams nothing and precomputes
+                               // the next step's update scalars
 };
 
 struct Pass2Args {
