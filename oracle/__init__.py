@@ -217,9 +217,11 @@ class Oracle:
         return d
 
     def update(self, d: Decision, s, master, m, v, p16, pdtype: int) -> None:
-        n = master.size
+        """master None: p16 is the master weight (low-precision masters)."""
+        n = m.size
+        assert master is not None or p16 is not None
         for a in (s, master, m, v):
-            assert a.size == n and a.dtype == np.float32
+            assert a is None or (a.size == n and a.dtype == np.float32)
         if p16 is not None:
             assert p16.size == n and p16.dtype == np.uint16
         self.L.orc_update(ctypes.byref(d), _ptr(s), _ptr(master), _ptr(m),
@@ -227,12 +229,14 @@ class Oracle:
 
     def step(self, hp: Hparams, st: Scaler, grads, gdtype: int, master, m, v,
              p16, pdtype: int, divisor: float, global_stats: Stats | None = None):
-        """One shard step in place; returns (own stats, decision)."""
-        n = master.size
+        """One shard step in place; returns (own stats, decision).  master
+        None: p16 is the master weight (low-precision masters)."""
+        n = m.size
+        assert master is not None or p16 is not None
         for g in grads:
             assert g.dtype == np.uint16 and g.size == n and g.flags["C_CONTIGUOUS"]
         for a in (master, m, v):
-            assert a.dtype == np.float32 and a.size == n and a.flags["C_CONTIGUOUS"]
+            assert a is None or (a.dtype == np.float32 and a.size == n and a.flags["C_CONTIGUOUS"])
         if p16 is not None:
             assert p16.dtype == np.uint16 and p16.size == n
         own = Stats()

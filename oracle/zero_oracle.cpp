@@ -296,7 +296,10 @@ extern "C" void orc_update(const orc_decision* d, const float* s, float* master,
   if (d->skip) return;
   for (int64_t j = 0; j < n; ++j) {
     const float g = s[j] * d->coef;
-    float mj = m[j], vj = v[j], pj = master[j];
+    // low-precision master weights: with no fp32 master array the 16-bit
+    // parameter is the master, widened here and rounded back below
+    float mj = m[j], vj = v[j];
+    float pj = master ? master[j] : orc_16_to_f32(p16[j], pdtype);
     mj = d->b1 * mj + d->omb1 * g;
     vj = d->b2 * vj + d->omb2 * (g * g);
     const float den = std::sqrt(vj) * d->isb2 + d->eps;
@@ -304,7 +307,7 @@ extern "C" void orc_update(const orc_decision* d, const float* s, float* master,
     pj = pj - d->step_size * (mj / den);
     m[j] = mj;
     v[j] = vj;
-    master[j] = pj;
+    if (master) master[j] = pj;
     if (p16) p16[j] = orc_f32_to_16(pj, pdtype);
   }
 }

@@ -113,7 +113,10 @@ orc_stats orc_fold_stats(const orc_stats* per_rank, int32_t n);
 void orc_decide(const orc_hparams* hp, orc_scaler* st, orc_stats global,
                 double divisor, orc_decision* out);
 
-/* a5..a7: unscale, clip, AdamW, 16-bit write-back over n elements. */
+/* a5..a7: unscale, clip, AdamW, 16-bit write-back over n elements.  With
+ * master == NULL the 16-bit copy p16 is the master weight (low-precision
+ * master weights): each element is widened to binary32, updated, and stored
+ * back rounded to nearest even. */
 void orc_update(const orc_decision* d, const float* s, float* master,
                 float* m, float* v, uint16_t* p16, int64_t n, int32_t pdtype);
 

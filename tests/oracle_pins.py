@@ -640,4 +640,56 @@ def pin_warmup_lr(orc):
     _close(master, -(1e-3 + 9e-3 / 4) * g / (np.abs(g) + 1e-8), 2e-6)
 
 
+def _m16_step(orc, p16_bits, lr, dtype, steps=1, fp32_master=False):
+    """`steps` steps at p with g = 1, beta1 = beta2 = 0, no bias correction,
+    wd = 0, scale 1, no clipping: each step is p - lr exactly (m = v = 1 and
+    den = 1 + 1e-8 rounds to 1 in binary32), then the 16-bit rounding."""
+    hp = O.hparams(lr=lr, betas=(0.0, 0.0), bias_correction=False)
+    st = O.scaler(1.0)
+    n = p16_bits.size
+    p16 = p16_bits.copy()
+    master = _f(p16, dtype).astype(np.float32) if fp32_master else None
+    m = np.zeros(n, np.float32)
+    v = np.zeros(n, np.float32)
+    one = np.full(n, 0x3C00 if dtype == F16 else 0x3F80, np.uint16)
+    for _ in range(steps):
+        orc.step(hp, st, [one], dtype, master, m, v, p16, dtype, 1.0)
+    return p16
+
+
+def pin_low_precision_master(orc):
+    """Low-precision master weights (reading R17: no fp32 master array, the
+    16-bit parameter is the master).  Closed forms from the formats' rounding
+    at p = 1 (each step computes p - lr exactly, see _m16_step):
+    bf16: lr 2^-4 gives 0.9375 = 0x3F70 exactly; lr 3*2^-10 gives
+    0.9970703125, nearest bf16 1 - 2^-8 = 0x3F7F; lr 2^-10 is within half an
+    ulp (2^-9) of 1 and is lost, every step, so 16 steps leave 0x3F80 where an
+    fp32 master reaches 1 - 2^-6 = 0x3F7C.  fp16: lr 2^-12 lands exactly
+    halfway between 1 and 1 - 2^-11 and ties to even, 0x3C00; lr 2^-10 gives
+    1 - 2^-10 = 0x3BFE exactly."""
+    one_b = np.array([0x3F80], np.uint16)
+    one_h = np.array([0x3C00], np.uint16)
+    assert _m16_step(orc, one_b, 2.0 ** -4, BF16)[0] == 0x3F70
+    assert _m16_step(orc, one_b, 3 * 2.0 ** -10, BF16)[0] == 0x3F7F
+    assert _m16_step(orc, one_b, 2.0 ** -10, BF16, steps=16)[0] == 0x3F80
+    assert _m16_step(orc, one_b, 2.0 ** -10, BF16, steps=16, fp32_master=True)[0] == 0x3F7C
+    assert _m16_step(orc, one_h, 2.0 ** -12, F16)[0] == 0x3C00
+    assert _m16_step(orc, one_h, 2.0 ** -10, F16)[0] == 0x3BFE
+
+
+def pin_low_precision_master_round_trip(orc):
+    """With lr = 0 a low-precision master keeps every finite 16-bit pattern
+    (widening is exact and p * 1 - 0 = p), in both formats."""
+    codes = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    for dtype, expmask in ((F16, 0x7C00), (BF16, 0x7F80)):
+        fin = codes[(codes & expmask) != expmask]
+        hp = O.hparams(lr=0.0, weight_decay=0.0)
+        n = fin.size
+        p16 = fin.copy()
+        g = np.full(n, 0x3C00 if dtype == F16 else 0x3F80, np.uint16)
+        orc.step(hp, O.scaler(1.0), [g], dtype, None, np.zeros(n, np.float32),
+                 np.zeros(n, np.float32), p16, dtype, 1.0)
+        assert (p16 == fin).all()
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -52,6 +52,12 @@ MUTANTS = [
     ("growth keeps the overflow count", "    st->clean = 0;\n    st->overflows = 0;\n  }", "    st->clean = 0;\n  }"),
     ("16-bit copy in the other format", "p16[j] = orc_f32_to_16(pj, pdtype);",
      "p16[j] = orc_f32_to_16(pj, 1 - pdtype);"),
+    ("low-precision master widened from the other format",
+     "float pj = master ? master[j] : orc_16_to_f32(p16[j], pdtype);",
+     "float pj = master ? master[j] : orc_16_to_f32(p16[j], 1 - pdtype);"),
+    ("low-precision master starts from zero",
+     "float pj = master ? master[j] : orc_16_to_f32(p16[j], pdtype);",
+     "float pj = master ? master[j] : 0.0f;"),
 ]
 
 
