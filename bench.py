@@ -22,6 +22,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -71,6 +72,12 @@ WORKLOADS = {
                        "2e-4 wd 0.01, clip 1.0",
                   numel=250_000_000, world=1, R=8, K=4, dtype="fp16", lr=2e-4, wd=0.01,
                   clip=1.0, dynamic=False, scale=1024.0, sigma=1e-3, seed=0x5EED0004),
+    "gpt2_master16": dict(desc="GPT-2-small-sized flat buffer, 124,439,808 params, N=1, bf16 grads "
+                               "~N(0,1e-2), bf16 low-precision master weights (no fp32 master), "
+                               "AdamW lr 3e-4 wd 0.01, global L2 clip 1.0, no loss scaling",
+                          numel=124_439_808, world=1, R=1, K=1, dtype="bf16", lr=3e-4, wd=0.01,
+                          clip=1.0, dynamic=False, scale=1.0, sigma=1e-2, seed=0x5EED0002,
+                          master16=True),
     "pertensor": dict(desc="per-tensor list: Llama-3-8B embedding + 8 decoder layers, 73 "
                            "tensors, 2,270,232,576 params, bf16 grads ~N(0,1e-3), AdamW lr 1e-4 "
                            "wd 0.1, clip 1.0",
@@ -103,14 +110,20 @@ def pass2_traffic_per_param():
     return float(mt.group(1))
 
 
+def state_bytes_per_param(w):
+    # fp32 master/m/v read + written + 16-bit copy written (26 B); with 16-bit
+    # masters: 16-bit master read, m/v read + written, 16-bit master written (20 B)
+    return 20 if w.get("master16") else 26
+
+
 def algorithmic_bytes_per_param(w):
-    # R*K 16-bit gradient reads + 12 B fp32 master/m/v read + 12 B written + 2 B 16-bit copy
-    return 2 * w["R"] * w["K"] + 12 + 12 + 2
+    # R*K 16-bit gradient reads + the optimizer state traffic
+    return 2 * w["R"] * w["K"] + state_bytes_per_param(w)
 
 
 def pass2_bytes_per_param(w, stash):
     # pass 2 alone: gradients (or the fp32 stash) read, state read and written, copy written
-    return (4 if stash else 2 * w["R"] * w["K"]) + 26
+    return (4 if stash else 2 * w["R"] * w["K"]) + state_bytes_per_param(w)
 
 
 class Setup:
@@ -130,7 +143,7 @@ class Setup:
         cfg = z.make_config(numel=w["numel"], world=w["world"], grad_dtype=code, lr=w["lr"],
                             weight_decay=w["wd"], max_grad_norm=w["clip"],
                             dynamic_scale=w["dynamic"], init_scale=w["scale"],
-                            scale_window=1000)
+                            scale_window=1000, master16=w.get("master16", False))
         self.h = z.zero_opt_create(cfg)
         nb = w["R"] * w["K"]
         self.stash = None
@@ -170,6 +183,8 @@ class Setup:
                 self.grads.append(g)
             if nb > 4:
                 self.stash = torch.empty(n, dtype=torch.float32, device=device)
+            if w.get("master16"):
+                self.master = None        # the 16-bit parameters are the masters
             self.bufs = z.make_buffers(self.master, self.m, self.v, self.p16_full, self.grads,
                                        n_ranks=w["R"], n_micro=w["K"], grads_shard_local=True,
                                        stash=self.stash)
@@ -190,8 +205,9 @@ class Setup:
             p2 = [it["param16"] for it in items2]
             return [(self.grads, self.p16, self.step),
                     (g2, p2, lambda sp, lst2=lst2: z.zero_opt_step_tensors(self.h, 0, lst2, sp))]
-        p16b = torch.empty_like(self.p16_full)
         w = self.w
+        # with 16-bit masters the parameters are optimizer state: one buffer
+        p16b = self.p16_full if w.get("master16") else torch.empty_like(self.p16_full)
         bufs2 = z.make_buffers(self.master, self.m, self.v, p16b, g2, n_ranks=w["R"],
                                n_micro=w["K"], grads_shard_local=True, stash=self.stash)
         b, e, _, _ = z.zero_opt_shard_bounds(self.h, 0)
@@ -401,6 +417,8 @@ def e2e_pipelined(setup, compute, steps):
             compute.wait_event(up[b])
             if down[b] is not None:
                 compute.wait_event(down[b])    # parameters of step i-2 downloaded
+            if setup.w.get("master16") and down[1 - b] is not None:
+                compute.wait_event(down[1 - b])  # one parameter buffer: step i-1's too
             sets[b][2](sp)
             done[b].record(compute)
             d2h.wait_event(done[b])
@@ -552,6 +570,57 @@ def run_ours(args):
     return 0
 
 
+def run_offload(args):
+    """The offloaded step (zero_host_step) of a flat workload on host buffers,
+    run by CPU threads: params/s over `--steps` steps after `--warmup`."""
+    import synth
+    import zero_sharded_mixed_05_gb300 as z
+    w = WORKLOADS[args.workload]
+    if args.workload == "pertensor":
+        raise SystemExit("--offload applies to flat workloads")
+    code = z.FP16 if w["dtype"] == "fp16" else z.BF16
+    kind = synth.F16 if code == z.FP16 else synth.BF16
+    cfg = z.make_config(numel=w["numel"], world=w["world"], grad_dtype=code, lr=w["lr"],
+                        weight_decay=w["wd"], max_grad_norm=w["clip"],
+                        dynamic_scale=w["dynamic"], init_scale=w["scale"], scale_window=1000,
+                        master16=w.get("master16", False))
+    h = z.zero_host_create(cfg, args.threads)
+    S = -(-w["numel"] // w["world"])
+    b, n = 0, min(S, w["numel"])                     # rank 0's shard
+    master = synth.normal_np(w["seed"], 0, b, n, 0.02, synth.F32)
+    p16 = z_cast16(master, code)
+    m = np.zeros(n, np.float32)
+    v = np.zeros(n, np.float32)
+    nb = w["R"] * w["K"]
+    grads = [synth.normal_np(w["seed"], 1 + i, b, n, w["sigma"] * w["scale"], kind)
+             for i in range(nb)]
+    bufs = z.make_buffers(None if w.get("master16") else master, m, v, p16, grads,
+                          n_ranks=w["R"], n_micro=w["K"], grads_shard_local=True,
+                          param16_shard_local=True)
+    for _ in range(args.warmup):
+        z.zero_host_step(h, 0, bufs)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        z.zero_host_step(h, 0, bufs)
+    dt = (time.perf_counter() - t0) / args.steps
+    threads = z.zero_host_threads(h)
+    z.zero_host_destroy(h)
+    print(json.dumps({
+        "metric": "offloaded optimizer-step params/s (host threads, host-resident state)",
+        "value": n / dt, "unit": "params/s", "impl": "offload", "threads": threads,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "dtype": "f32", "data": "synthetic",
+        "host_gbs": algorithmic_bytes_per_param(w) * n / dt / 1e9,
+        "config": {"workload": w["desc"], "params": n, "cpu": platform.machine()}}))
+
+
+def z_cast16(x, code):
+    """Host 16-bit copy (round to nearest even) of fp32 values, via torch."""
+    import torch
+    dt = torch.float16 if code == 0 else torch.bfloat16
+    return torch.from_numpy(x).to(dt).view(torch.int16).numpy().view(np.uint16).copy()
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -563,6 +632,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--numel", type=int, default=0,
                     help="override the flat workload's parameters per shard (profiling runs)")
+    ap.add_argument("--offload", action="store_true",
+                    help="time the offloaded step (CPU threads, host buffers) instead")
+    ap.add_argument("--threads", type=int, default=0,
+                    help="threads of the offloaded step (0: all hardware threads)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -575,6 +648,8 @@ def main():
         WORKLOADS[args.workload] = w
     if args.impl == "reference":
         return run_reference(args)
+    if args.offload:
+        return run_offload(args)
     return run_ours(args)
 
 

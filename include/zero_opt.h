@@ -97,6 +97,13 @@ typedef struct zero_opt_config {
   double warmup_min_lr;     /* WarmupLR: update t uses warmup_min_lr +      */
   double warmup_max_lr;     /*   (max - min) * min(t, T) / T, T =           */
   int64_t warmup_num_steps; /*   warmup_num_steps; 0 keeps lr constant      */
+  int32_t master16;         /* 1: low-precision master weights -- no fp32
+                               master array (buffers' master is ignored, may
+                               be NULL); the 16-bit parameter is the master,
+                               widened to fp32 for the update and stored back
+                               rounded to nearest even ("LLM-train tutorials
+                               ch01" §1.7).  0: fp32 master (default)        */
+  int32_t reserved;         /* 0                                            */
 } zero_opt_config;
 
 /*
@@ -359,7 +366,8 @@ zero_status zero_opt_ckpt_read(const char* path, zero_opt_ckpt_info* info,
 
 /* Save `rank`'s shard: its DEVICE master, m and v (shard-local; the first
  * real_len elements are stored) and its loss-scaler replica.  Synchronizes
- * `stream`.  Errors: as zero_opt_ckpt_write, plus ERANGE (rank), ECUDA. */
+ * `stream`.  Errors: as zero_opt_ckpt_write, plus ERANGE (rank), ECUDA,
+ * ENOTSUP (a master16 handle: it has no fp32 master weights to store). */
 zero_status zero_opt_save_shard(zero_opt_t h, int32_t rank, const float* master,
                                 const float* m, const float* v, void* stream,
                                 const char* path);
@@ -370,7 +378,7 @@ zero_status zero_opt_save_shard(zero_opt_t h, int32_t rank, const float* master,
  * slice of the 16-bit parameter copy as the rounding of the restored master
  * weights (param16 is the full padded buffer unless param16_shard_local).
  * Synchronizes `stream`.  Errors: EINVAL (file for another numel/world/rank,
- * unreadable or corrupt file), ERANGE, ECUDA. */
+ * unreadable or corrupt file), ERANGE, ECUDA, ENOTSUP (a master16 handle). */
 zero_status zero_opt_load_shard(zero_opt_t h, int32_t rank, float* master, float* m,
                                 float* v, void* param16, int32_t param16_shard_local,
                                 void* stream, const char* path);

@@ -65,20 +65,24 @@ class Run:
         # the oracle's statistics of every chunk of every group, in list order;
         # the gradients do not change between steps except for the injection
         self.chunks = []
-        for gi, (master, _, _, _, grads) in enumerate(self.groups):
-            n = master.numel()
+        for gi, (_, m, _, _, grads) in enumerate(self.groups):
+            n = m.numel()
             for c0 in range(0, n, CHUNK):
                 c1 = min(n, c0 + CHUNK)
                 self.chunks.append((gi, c0, c1, _chunk_stats(self.orc, grads, self.code, c0, c1)))
         self.samples = []
-        for gi, (master, m, v, _, _) in enumerate(self.groups):
-            n = master.numel()
+        for gi, (master, m, v, p16, _) in enumerate(self.groups):
+            n = m.numel()
             idx = _sample(n, 1000 + gi, 60_000 if len(self.groups) == 1 else 2_000)
             ti = torch.from_numpy(idx).cuda()
-            self.samples.append(dict(ti=ti, master=master[ti].cpu().numpy().copy(),
+            # with 16-bit masters (master None) the parameters are the state
+            self.samples.append(dict(ti=ti,
+                                     master=None if master is None
+                                     else master[ti].cpu().numpy().copy(),
                                      m=m[ti].cpu().numpy().copy(),
                                      v=v[ti].cpu().numpy().copy(),
-                                     p16=np.zeros(idx.size, np.uint16)))
+                                     p16=to_np16(p16[ti]) if master is None
+                                     else np.zeros(idx.size, np.uint16)))
 
     def step(self, inject=None):
         """One GPU step and the oracle on the sample."""
@@ -109,7 +113,8 @@ class Run:
     def check(self):
         for smp, (master, m, v, p16, _) in zip(self.samples, self.groups):
             ti = smp["ti"]
-            assert_state("master", master[ti].cpu().numpy(), smp["master"])
+            if master is not None:
+                assert_state("master", master[ti].cpu().numpy(), smp["master"])
             assert_state("m", m[ti].cpu().numpy(), smp["m"])
             assert_state("v", v[ti].cpu().numpy(), smp["v"])
             assert ulp16_diff(to_np16(p16[ti]), smp["p16"]) <= 1
@@ -148,3 +153,7 @@ def test_fullsize_fused_reduce():
 
 def test_fullsize_per_tensor_list():
     _run("pertensor")
+
+
+def test_fullsize_gpt2_low_precision_master():
+    _run("gpt2_master16")

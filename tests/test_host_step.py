@@ -30,7 +30,7 @@ def run_host(z, orc, *, numel, world=1, R=1, K=1, gdtype=O.FP16, pdtype=None, st
              threads=3, lr=1e-3, wd=0.0, max_norm=0.0, dynamic=False, init_scale=1.0,
              window=1000, hysteresis=1, warmup=(0.0, 0.0, 0), sigma=1e-3, seed=0x5EED0101,
              inject=None, grads_local=False, p16_local=False, divisor=0.0,
-             master=None, bias_correction=True):
+             master=None, bias_correction=True, master16=False):
     """Step every rank of a `world`-way sharded buffer `steps` times on the host
     and with the oracle; assert bit-identical results after every step."""
     pdtype = gdtype if pdtype is None else pdtype
@@ -38,7 +38,7 @@ def run_host(z, orc, *, numel, world=1, R=1, K=1, gdtype=O.FP16, pdtype=None, st
     cfg = z.make_config(numel=numel, world=world, grad_dtype=gdtype, param_dtype=pdtype, lr=lr,
                         weight_decay=wd, max_grad_norm=max_norm, dynamic_scale=dynamic,
                         init_scale=init_scale, scale_window=window, hysteresis=hysteresis,
-                        warmup=warmup, bias_correction=bias_correction)
+                        warmup=warmup, bias_correction=bias_correction, master16=master16)
     hp = O.hparams(lr=lr, weight_decay=wd, max_grad_norm=max_norm, dynamic_scale=dynamic,
                    scale_window=window, hysteresis=hysteresis, warmup=warmup,
                    bias_correction=bias_correction)
@@ -49,15 +49,21 @@ def run_host(z, orc, *, numel, world=1, R=1, K=1, gdtype=O.FP16, pdtype=None, st
     bounds = [orc.shard_bounds(numel, world, r) for r in range(world)]
     p0 = master if master is not None else synth.normal_np(seed, 0, 0, numel, 0.02, synth.F32)
     st, ref, osc = [], [], []
+    p16 = np.zeros(P, np.uint16)
+    p16_loc = [np.zeros(S, np.uint16) for _ in range(world)]
+    q0 = orc.f32_to_16(p0, pdtype) if master16 else None   # the 16-bit masters
     for r in range(world):
         b, e, _, _ = bounds[r]
         st.append([np.zeros(S, np.float32) for _ in range(3)])
         st[r][0][:e - b] = p0[b:e]
-        ref.append([p0[b:e].copy(), np.zeros(e - b, np.float32), np.zeros(e - b, np.float32),
-                    np.zeros(e - b, np.uint16)])
+        ref.append([None if master16 else p0[b:e].copy(), np.zeros(e - b, np.float32),
+                    np.zeros(e - b, np.float32),
+                    q0[b:e].copy() if master16 else np.zeros(e - b, np.uint16)])
         osc.append(O.scaler(init_scale))
-    p16 = np.zeros(P, np.uint16)
-    p16_loc = [np.zeros(S, np.uint16) for _ in range(world)]
+        if master16:
+            p16[b:e] = q0[b:e]
+            p16_loc[r][:e - b] = q0[b:e]
+            st[r][0] = None
     decisions = []
     for step in range(1, steps + 1):
         scale = osc[0].scale
@@ -81,7 +87,8 @@ def run_host(z, orc, *, numel, world=1, R=1, K=1, gdtype=O.FP16, pdtype=None, st
                     gl.append(loc)
             else:
                 gl = grads
-            bufs.append(z.make_buffers(*st[r], p16_loc[r] if p16_local else p16, gl,
+            bufs.append(z.make_buffers(st[r][0], st[r][1], st[r][2],
+                                       p16_loc[r] if p16_local else p16, gl,
                                        n_ranks=R, n_micro=K, grads_shard_local=grads_local,
                                        param16_shard_local=p16_local, divisor=divisor))
         per = [z.zero_host_grad_stats(h, r, bufs[r]) for r in range(world)]
@@ -108,10 +115,12 @@ def run_host(z, orc, *, numel, world=1, R=1, K=1, gdtype=O.FP16, pdtype=None, st
             b, e, _, _ = bounds[r]
             assert z.zero_host_loss_scale(h, r).as_tuple() == osc[r].as_tuple(), (step, r)
             for a, o, name in zip(st[r][:3], ref[r][:3], ("master", "m", "v")):
+                if o is None:
+                    continue
                 assert (a[:e - b].view(np.uint32) == o.view(np.uint32)).all(), (step, r, name)
             got16 = p16_loc[r][:e - b] if p16_local else p16[b:e]
             assert (got16 == ref[r][3]).all(), (step, r, "param16")
-            assert not st[r][0][e - b:].any()          # padding of the state untouched
+            assert not st[r][1][e - b:].any()          # padding of the state untouched
         if not p16_local:
             assert not p16[numel:].any()               # padding of the parameters untouched
         decisions.append((dec.skip, dec.scale_used))
@@ -189,3 +198,12 @@ def test_host_errors(z):
     assert e.value.status == z.ZERO_EINVAL
     assert z.zero_host_threads(h) == 2
     z.zero_host_destroy(h)
+
+
+@pytest.mark.parametrize("pdtype", [O.BF16, O.FP16])
+def test_low_precision_master(z, orc, pdtype):
+    """master16: the 16-bit parameters are the master weights (no fp32 array);
+    clipping, weight decay and an overflow step included."""
+    run_host(z, orc, numel=60_001, world=2, R=2, gdtype=O.BF16, pdtype=pdtype, steps=5,
+             threads=3, lr=1e-3, wd=0.01, max_norm=0.5, sigma=1e-2, dynamic=True,
+             init_scale=4.0, inject={3: [(1, 4242, 0x7F80)]}, master16=True)

@@ -335,3 +335,26 @@ def test_hysteresis_and_warmup_lr():
     res = run_flat(case)
     assert [h["gpu"][0] for h in res["history"]] == [int(s in inj) for s in range(1, 15)]
     assert_flat_parity(res)
+
+
+@pytest.mark.parametrize("gdtype", [O.BF16, O.FP16])
+def test_low_precision_master(gdtype):
+    """master16: no fp32 master array, the 16-bit parameters are the masters
+    (widened, updated, stored back rounded).  Two shards, clipping, weight
+    decay, dynamic scale with an overflow on step 3; the 16-bit masters must
+    match the oracle's within one ulp and m, v within the state tolerance."""
+    inj = {3: [(1, 777, INF16 if gdtype == O.FP16 else 0x7F80)]}
+    case = FlatCase(numel=300_007, world=2, ranks=2, gdtype=gdtype, lr=1e-3, wd=0.01,
+                    max_norm=0.5, dynamic=True, init_scale=16.0, sigma=1e-2, steps=5,
+                    inject=inj, master16=True)
+    res = run_flat(case)
+    assert [h["gpu"][0] for h in res["history"]] == [0, 0, 1, 0, 0]
+    assert_flat_parity(res)
+    # the 16-bit masters agree bit for bit on at least 99.9% of the elements
+    same = tot = 0
+    for r in res["gpu"]:
+        g16 = res["gpu"][r][0].view(np.uint32)
+        o16 = res["ref"][r][0].view(np.uint32)
+        same += int((g16 == o16).sum())
+        tot += g16.size
+    assert same >= 0.999 * tot, same / tot

@@ -34,7 +34,7 @@ class zero_opt_config(ctypes.Structure):
                 ("dynamic_scale", _i32), ("hysteresis", _i32),
                 ("init_scale", _f64), ("min_scale", _f64), ("scale_factor", _f64),
                 ("scale_window", _i64), ("warmup_min_lr", _f64), ("warmup_max_lr", _f64),
-                ("warmup_num_steps", _i64)]
+                ("warmup_num_steps", _i64), ("master16", _i32), ("reserved", _i32)]
 
 
 class zero_opt_buffers(ctypes.Structure):
@@ -199,9 +199,10 @@ def make_config(numel=0, world=1, grad_dtype=FP16, param_dtype=None, lr=2e-5,
                 betas=(0.9, 0.999), eps=1e-8, weight_decay=0.01, max_grad_norm=0.0,
                 bias_correction=True, dynamic_scale=True, init_scale=65536.0,
                 min_scale=1.0, scale_factor=2.0, scale_window=1000,
-                hysteresis=1, warmup=(0.0, 0.0, 0)) -> zero_opt_config:
+                hysteresis=1, warmup=(0.0, 0.0, 0), master16=False) -> zero_opt_config:
     """`warmup` = (warmup_min_lr, warmup_max_lr, warmup_num_steps); 0 steps
-    keeps lr constant."""
+    keeps lr constant.  `master16`: the 16-bit parameters are the master
+    weights (no fp32 master array)."""
     cfg = zero_opt_config()
     _check(lib().zero_opt_config_default(ctypes.byref(cfg)), "zero_opt_config_default")
     cfg.numel = numel
@@ -221,6 +222,7 @@ def make_config(numel=0, world=1, grad_dtype=FP16, param_dtype=None, lr=2e-5,
     cfg.scale_window = scale_window
     cfg.hysteresis = hysteresis
     cfg.warmup_min_lr, cfg.warmup_max_lr, cfg.warmup_num_steps = warmup
+    cfg.master16 = int(master16)
     return cfg
 
 

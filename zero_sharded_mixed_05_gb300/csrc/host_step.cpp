@@ -256,16 +256,28 @@ void stats_range(const Job& jb, int64_t lo, int64_t hi, Partial* out) {
 
 void update_range(const Job& jb, const zo::Decision& d, int64_t lo, int64_t hi) {
   alignas(64) float s[kBlock];
+  alignas(64) float pw[kBlock];  // widened 16-bit masters (master16)
   const bool half16 = jb.cfg->param_dtype == ZERO_FP16;
+  const bool m16 = jb.cfg->master16 != 0;
+  const float* tab = half_table().v;
   const float coef = d.coef, b1 = d.b1, omb1 = d.omb1, b2 = d.b2, omb2 = d.omb2;
   const float isb2 = d.isb2, eps = d.eps, decay = d.decay, step_size = d.step_size;
   for (int64_t j0 = lo; j0 < hi; j0 += kBlock) {
     const int64_t len = std::min(kBlock, hi - j0);
     reduce_block(jb, j0, len, s);
-    float* __restrict__ P = jb.master + j0;
+    uint16_t* __restrict__ Q = jb.p16 + j0;
+    // low-precision master weights: the 16-bit parameter, widened, is the
+    // master; pw holds it for the block and is not stored back
+    float* __restrict__ P = m16 ? pw : jb.master + j0;
+    if (m16) {
+      if (half16) {
+        for (int64_t k = 0; k < len; ++k) pw[k] = tab[Q[k]];
+      } else {
+        for (int64_t k = 0; k < len; ++k) pw[k] = bf16_to_f32(Q[k]);
+      }
+    }
     float* __restrict__ M = jb.m + j0;
     float* __restrict__ V = jb.v + j0;
-    uint16_t* __restrict__ Q = jb.p16 + j0;
     for (int64_t k = 0; k < len; ++k) {
       const float g = s[k] * coef;
       const float mk = b1 * M[k] + omb1 * g;
@@ -319,8 +331,8 @@ zero_status make_job(zero_host_t h, int32_t rank, const zero_opt_buffers* b, boo
   if (real > 0) {
     for (int64_t k = 0; k < nbuf; ++k)
       if (!b->grads[k]) return fail(ZERO_EINVAL, "gradient pointer %lld is NULL", (long long)k);
-    if (need_state && (!b->master || !b->m || !b->v || !b->param16))
-      return fail(ZERO_EINVAL, "master, m, v and param16 must not be NULL");
+    if (need_state && ((!h->cfg.master16 && !b->master) || !b->m || !b->v || !b->param16))
+      return fail(ZERO_EINVAL, "master (unless master16), m, v and param16 must not be NULL");
   }
   g->resize((size_t)nbuf);
   const int64_t goff = b->grads_shard_local ? 0 : begin;
@@ -330,7 +342,7 @@ zero_status make_job(zero_host_t h, int32_t rank, const zero_opt_buffers* b, boo
   jb->g = g->data();
   jb->nbuf = (int)nbuf;
   jb->n = real;
-  jb->master = b->master;
+  jb->master = h->cfg.master16 ? nullptr : b->master;
   jb->m = b->m;
   jb->v = b->v;
   jb->p16 = b->param16 ? static_cast<uint16_t*>(b->param16) + (b->param16_shard_local ? 0 : begin)

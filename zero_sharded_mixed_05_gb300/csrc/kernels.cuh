@@ -790,7 +790,9 @@ __device__ __forceinline__ void f4_to(const float4& a, float* d) {
 }
 
 // SRC == 1: one gradient buffer; SRC == 0: a.nbuf buffers; SRC == -1: stash.
-template <typename GT, typename PT, int SRC>
+// M16: low-precision master weights -- there is no fp32 master array; the
+// 16-bit parameter is widened, updated and stored back rounded.
+template <typename GT, typename PT, int SRC, bool M16>
 __global__ void __launch_bounds__(kThreads, ZO_PASS2_MIN_CTAS) pass2_kernel(const Pass2Args a) {
   const Decision* dp = a.dec;
   if (dp->skip) return;
@@ -845,28 +847,34 @@ __global__ void __launch_bounds__(kThreads, ZO_PASS2_MIN_CTAS) pass2_kernel(cons
           }
         }
       }
-      const float4* pm = reinterpret_cast<const float4*>(s.master + e0);
+      unsigned short* p16 = static_cast<unsigned short*>(s.p16) + e0;
+      if (M16) {
+        Fmt<PT>::dec8(__ldcs(reinterpret_cast<const uint4*>(p16)), p);
+      } else {
+        const float4* pm = reinterpret_cast<const float4*>(s.master + e0);
+        f4_to(__ldcs(pm), p);
+        f4_to(__ldcs(pm + 1), p + 4);
+      }
       const float4* mm = reinterpret_cast<const float4*>(s.m + e0);
       const float4* vm = reinterpret_cast<const float4*>(s.v + e0);
-      f4_to(__ldcs(pm), p);
-      f4_to(__ldcs(pm + 1), p + 4);
       f4_to(__ldcs(mm), m);
       f4_to(__ldcs(mm + 1), m + 4);
       f4_to(__ldcs(vm), v);
       f4_to(__ldcs(vm + 1), v + 4);
 #pragma unroll
       for (int i = 0; i < kVec; ++i) adam_elem(x[i], p[i], m[i], v[i], c);
-      float4* po = reinterpret_cast<float4*>(s.master + e0);
+      if (!M16) {
+        float4* po = reinterpret_cast<float4*>(s.master + e0);
+        __stcs(po, make_float4(p[0], p[1], p[2], p[3]));
+        __stcs(po + 1, make_float4(p[4], p[5], p[6], p[7]));
+      }
       float4* mo = reinterpret_cast<float4*>(s.m + e0);
       float4* vo = reinterpret_cast<float4*>(s.v + e0);
-      __stcs(po, make_float4(p[0], p[1], p[2], p[3]));
-      __stcs(po + 1, make_float4(p[4], p[5], p[6], p[7]));
       __stcs(mo, make_float4(m[0], m[1], m[2], m[3]));
       __stcs(mo + 1, make_float4(m[4], m[5], m[6], m[7]));
       __stcs(vo, make_float4(v[0], v[1], v[2], v[3]));
       __stcs(vo + 1, make_float4(v[4], v[5], v[6], v[7]));
-      __stcs(reinterpret_cast<uint4*>(static_cast<unsigned short*>(s.p16) + e0),
-             Fmt<PT>::enc8(p));
+      __stcs(reinterpret_cast<uint4*>(p16), Fmt<PT>::enc8(p));
     } else {
 #pragma unroll
       for (int i = 0; i < kVec; ++i) {
@@ -880,12 +888,14 @@ __global__ void __launch_bounds__(kThreads, ZO_PASS2_MIN_CTAS) pass2_kernel(cons
           for (int b = 0; b < a.nbuf; ++b)
             x = __fadd_rn(x, Fmt<GT>::dec(__ldcs(grad_ptr(a.gptrs, s, b) + e)));
         }
-        float p = __ldcs(s.master + e), m = __ldcs(s.m + e), v = __ldcs(s.v + e);
+        unsigned short* p16 = static_cast<unsigned short*>(s.p16) + e;
+        float p = M16 ? Fmt<PT>::dec(*p16) : __ldcs(s.master + e);
+        float m = __ldcs(s.m + e), v = __ldcs(s.v + e);
         adam_elem(x, p, m, v, c);
-        __stcs(s.master + e, p);
+        if (!M16) __stcs(s.master + e, p);
         __stcs(s.m + e, m);
         __stcs(s.v + e, v);
-        static_cast<unsigned short*>(s.p16)[e] = Fmt<PT>::enc(p);
+        *p16 = Fmt<PT>::enc(p);
       }
     }
   }

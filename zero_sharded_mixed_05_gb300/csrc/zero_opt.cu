@@ -79,6 +79,7 @@ zero_status check_config(const zero_opt_config* c) {
   if (c->hysteresis < 1) return fail(ZERO_EINVAL, "hysteresis must be >= 1");
   if (c->warmup_num_steps < 0 || !(c->warmup_min_lr >= 0.0) || !(c->warmup_max_lr >= 0.0))
     return fail(ZERO_EINVAL, "warm-up steps and learning rates must be >= 0");
+  if (c->master16 != 0 && c->master16 != 1) return fail(ZERO_EINVAL, "master16 must be 0 or 1");
   return ZERO_OK;
 }
 
@@ -330,19 +331,24 @@ Pass1Fn pick_pass1(int gdt, bool stash, bool one, int64_t ntiles) {
                : zo::pass1_multi_kernel<__nv_bfloat16, false>;
 }
 
-template <typename GT, typename PT>
-Pass2Fn pick_pass2_t(int src) {
-  if (src == -1) return zo::pass2_kernel<GT, PT, -1>;
-  if (src == 1) return zo::pass2_kernel<GT, PT, 1>;
-  return zo::pass2_kernel<GT, PT, 0>;
+template <typename GT, typename PT, bool M16>
+Pass2Fn pick_pass2_src(int src) {
+  if (src == -1) return zo::pass2_kernel<GT, PT, -1, M16>;
+  if (src == 1) return zo::pass2_kernel<GT, PT, 1, M16>;
+  return zo::pass2_kernel<GT, PT, 0, M16>;
 }
 
-Pass2Fn pick_pass2(int gdt, int pdt, int src) {
+template <typename GT, typename PT>
+Pass2Fn pick_pass2_t(int src, bool m16) {
+  return m16 ? pick_pass2_src<GT, PT, true>(src) : pick_pass2_src<GT, PT, false>(src);
+}
+
+Pass2Fn pick_pass2(int gdt, int pdt, int src, bool m16) {
   if (gdt == ZERO_FP16)
-    return pdt == ZERO_FP16 ? pick_pass2_t<__half, __half>(src)
-                            : pick_pass2_t<__half, __nv_bfloat16>(src);
-  return pdt == ZERO_FP16 ? pick_pass2_t<__nv_bfloat16, __half>(src)
-                          : pick_pass2_t<__nv_bfloat16, __nv_bfloat16>(src);
+    return pdt == ZERO_FP16 ? pick_pass2_t<__half, __half>(src, m16)
+                            : pick_pass2_t<__half, __nv_bfloat16>(src, m16);
+  return pdt == ZERO_FP16 ? pick_pass2_t<__nv_bfloat16, __half>(src, m16)
+                          : pick_pass2_t<__nv_bfloat16, __nv_bfloat16>(src, m16);
 }
 
 
@@ -423,7 +429,7 @@ zero_status run(zero_opt_t h, int32_t rank, const std::vector<HostRun>& runs, in
   a2.dec = &h->ws->dec;
   const int src = use_stash ? -1 : (nbuf == 1 ? 1 : 0);
   const void* f2 = reinterpret_cast<const void*>(
-      pick_pass2(h->cfg.grad_dtype, h->cfg.param_dtype, src));
+      pick_pass2(h->cfg.grad_dtype, h->cfg.param_dtype, src, h->cfg.master16 != 0));
   int64_t g2 = (int64_t)occupancy(h, f2) * h->sms;
   g2 = std::min<int64_t>(g2, plan->ntiles);
   st = launch_kernel(h, f2, (int)g2, &a2, stream);
@@ -459,14 +465,15 @@ zero_status flat_runs(zero_opt_t h, int32_t rank, const zero_opt_buffers* b,
   const int64_t n = end - begin;
   st = check_grads(b->grads, nb, n > 0);
   if (st != ZERO_OK) return st;
-  if (n > 0 && (!b->master || !b->m || !b->v || !b->param16))
-    return fail(ZERO_EINVAL, "master, m, v and param16 must be non-NULL");
+  const bool m16 = h->cfg.master16 != 0;
+  if (n > 0 && ((!m16 && !b->master) || !b->m || !b->v || !b->param16))
+    return fail(ZERO_EINVAL, "master (unless master16), m, v and param16 must be non-NULL");
   *nbuf = nb;
   *divisor = b->divisor > 0.0 ? b->divisor : (double)nb;
   runs->clear();
   if (n == 0) return ZERO_OK;
   HostRun r;
-  r.master = b->master;
+  r.master = m16 ? nullptr : b->master;
   r.m = b->m;
   r.v = b->v;
   r.p16 = static_cast<unsigned char*>(b->param16) + (b->param16_shard_local ? 0 : begin * 2);
@@ -479,8 +486,8 @@ zero_status flat_runs(zero_opt_t h, int32_t rank, const zero_opt_buffers* b,
   return ZERO_OK;
 }
 
-zero_status list_runs(const zero_opt_tensor_list* l, std::vector<HostRun>* runs, int* nbuf,
-                      double* divisor) {
+zero_status list_runs(const zero_opt_tensor_list* l, bool m16, std::vector<HostRun>* runs,
+                      int* nbuf, double* divisor) {
   if (!l) return fail(ZERO_EINVAL, "tensor list is NULL");
   if (l->n_tensors < 0) return fail(ZERO_EINVAL, "n_tensors must be >= 0");
   if (l->n_tensors > 0 && !l->tensors) return fail(ZERO_EINVAL, "tensors array is NULL");
@@ -493,12 +500,13 @@ zero_status list_runs(const zero_opt_tensor_list* l, std::vector<HostRun>* runs,
     const zero_opt_tensor& t = l->tensors[i];
     if (t.numel < 0) return fail(ZERO_EINVAL, "tensor %d has numel < 0", i);
     if (t.numel > 0) {
-      if (!t.master || !t.m || !t.v || !t.param16)
-        return fail(ZERO_EINVAL, "tensor %d: master, m, v and param16 must be non-NULL", i);
+      if ((!m16 && !t.master) || !t.m || !t.v || !t.param16)
+        return fail(ZERO_EINVAL,
+                    "tensor %d: master (unless master16), m, v and param16 must be non-NULL", i);
       st = check_grads(t.grads, nb, true);
       if (st != ZERO_OK) return st;
       HostRun r;
-      r.master = t.master;
+      r.master = m16 ? nullptr : t.master;
       r.m = t.m;
       r.v = t.v;
       r.p16 = t.param16;
@@ -721,7 +729,7 @@ zero_status zero_opt_grad_stats_tensors(zero_opt_t h, int32_t rank,
   std::vector<HostRun> runs;
   int nbuf = 0;
   double divisor = 1.0;
-  st = list_runs(list, &runs, &nbuf, &divisor);
+  st = list_runs(list, h->cfg.master16 != 0, &runs, &nbuf, &divisor);
   if (st != ZERO_OK) return st;
   st = check_device(h);
   if (st != ZERO_OK) return st;
@@ -747,7 +755,7 @@ zero_status zero_opt_step_tensors(zero_opt_t h, int32_t rank, const zero_opt_ten
   std::vector<HostRun> runs;
   int nbuf = 0;
   double divisor = 1.0;
-  st = list_runs(list, &runs, &nbuf, &divisor);
+  st = list_runs(list, h->cfg.master16 != 0, &runs, &nbuf, &divisor);
   if (st != ZERO_OK) return st;
   st = check_device(h);
   if (st != ZERO_OK) return st;
@@ -803,6 +811,8 @@ zero_status zero_opt_save_shard(zero_opt_t h, int32_t rank, const float* master,
                                 const char* path) {
   zero_status st = check_handle_rank(h, rank);
   if (st != ZERO_OK) return st;
+  if (h->cfg.master16)
+    return fail(ZERO_ENOTSUP, "shard files hold fp32 master weights; a master16 handle has none");
   if (!path) return fail(ZERO_EINVAL, "path is NULL");
   zero_opt_ckpt_info info;
   std::memset(&info, 0, sizeof(info));
@@ -836,6 +846,8 @@ zero_status zero_opt_load_shard(zero_opt_t h, int32_t rank, float* master, float
                                 void* stream, const char* path) {
   zero_status st = check_handle_rank(h, rank);
   if (st != ZERO_OK) return st;
+  if (h->cfg.master16)
+    return fail(ZERO_ENOTSUP, "shard files hold fp32 master weights; a master16 handle has none");
   if (!path) return fail(ZERO_EINVAL, "path is NULL");
   zero_opt_ckpt_info info;
   st = zero_opt_ckpt_read(path, &info, nullptr, nullptr, nullptr);
