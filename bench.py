@@ -436,6 +436,66 @@ def e2e_pipelined(setup, compute, steps):
     return run(steps)
 
 
+def link_rates(setup, reps=3):
+    """GB/s of the step's own transfers with nothing else running: the
+    gradients host->device alone, the 16-bit parameters device->host alone,
+    and both at once on two streams (bytes of both / time), best of `reps`."""
+    import torch
+    host_g = [torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in setup.grads]
+    for hg, g in zip(host_g, setup.grads):
+        hg.copy_(g)                       # the uploads write back the same gradients
+    host_p = [torch.empty(p.shape, dtype=p.dtype, pin_memory=True) for p in setup.p16]
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def timed(up, down):
+        best = float("inf")
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            cur = torch.cuda.current_stream()
+            a.record(cur)
+            s1.wait_stream(cur)
+            s2.wait_stream(cur)
+            if up:
+                with torch.cuda.stream(s1):
+                    for hg, g in zip(host_g, setup.grads):
+                        g.copy_(hg, non_blocking=True)
+            if down:
+                with torch.cuda.stream(s2):
+                    for hp_, p in zip(host_p, setup.p16):
+                        hp_.copy_(p, non_blocking=True)
+            cur.wait_stream(s1)
+            cur.wait_stream(s2)
+            b.record(cur)
+            torch.cuda.synchronize()
+            best = min(best, a.elapsed_time(b) * 1e-3)
+        return best
+
+    bi, bo = setup.input_bytes(), setup.output_bytes()
+    return {"h2d_gbs": bi / timed(True, False) / 1e9, "d2h_gbs": bo / timed(False, True) / 1e9,
+            "both_gbs": (bi + bo) / timed(True, True) / 1e9}
+
+
+def d2d_copy_gbs(dev, nbytes=1 << 30, reps=5):
+    """A large device-to-device copy (cudaMemcpyAsync through torch), read +
+    write bytes / time, best of `reps`: the achievable copy ceiling."""
+    import torch
+    a = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    b = torch.empty_like(a)
+    best = float("inf")
+    for _ in range(reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        b.copy_(a)
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1) * 1e-3)
+    del a, b
+    return 2 * nbytes / best / 1e9
+
+
 def run_ours(args):
     import torch
     ws, rank, local = dist_env()
@@ -523,6 +583,8 @@ def run_ours(args):
     if ws > 1:
         e2e_ms = max_over_ranks(e2e_ms, dev)
     e2e_value = ws * n / (e2e_ms * 1e-3)
+    links = link_rates(setup)
+    d2d = d2d_copy_gbs(dev)
 
     tpp = pass2_traffic_per_param() if (args.workload == "gpt2" and not stash) else None
     traffic = tpp * n if tpp is not None else None
@@ -547,6 +609,7 @@ def run_ours(args):
                        "l2": "inputs larger than L2 (algorithmic %.2f GB per step)" % (step_bytes / 1e9),
                        "stash": stash},
             "hbm_gbs": step_gbs, "hbm_frac": step_gbs / peak,
+            "d2d_copy_gbs": d2d,
             "algorithmic_bytes_per_param": algorithmic_bytes_per_param(w),
             "roofline": {"bound": "hbm", "kernel": "pass2_kernel (unscale+clip+AdamW+cast)",
                          "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -558,7 +621,8 @@ def run_ours(args):
                     "h2d_bytes_per_step": setup.input_bytes(),
                     "d2h_bytes_per_step": setup.output_bytes(), "ms_per_step": e2e_ms,
                     "transfers": "pinned host buffers; H2D and D2H on their own streams, "
-                                 "double-buffered device copies, overlapped with the steps"},
+                                 "double-buffered device copies, overlapped with the steps",
+                    "link_gbs": links},
             "gpu_launches": launches,
             "clocks": clk,
         }
