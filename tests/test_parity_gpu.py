@@ -358,3 +358,13 @@ def test_low_precision_master(gdtype):
         same += int((g16 == o16).sum())
         tot += g16.size
     assert same >= 0.999 * tot, same / tot
+
+
+@pytest.mark.parametrize("stash", [True, False])
+def test_low_precision_master_tensor_list(stash):
+    """master16 on a per-tensor list with R*K = 2*3 fp16 buffers (the
+    multi-buffer pass 1, and the stash when asked), ragged tensor sizes."""
+    res = run_list([5000, 2049, 1, 70_001, 4096], gdtype=O.FP16, lr=1e-3, wd=0.01,
+                   max_norm=0.5, sigma=1e-3, steps=3, ranks=2, micro=3, stash=stash,
+                   master16=True)
+    assert_flat_parity(res)

@@ -193,10 +193,12 @@ __device__ __forceinline__ const unsigned short* grad_ptr(const void* const* gpt
 // element.  Each square is therefore formed exactly as p + e (p = s*s rounded,
 // e = fma(s, s, -p)) and added into a per-thread double-binary32 accumulator
 // (hi, lo) with Knuth's TwoSum; even and odd elements go to two independent
-// accumulators so consecutive additions do not wait on each other.  The
-// thread's total hi + lo is taken in binary64; the accumulated error is a few
-// units of 2^-48 of the thread's sum.  Every operation is an explicit IEEE
-// round-to-nearest intrinsic, so nothing is contracted.  Tiles whose largest
+// accumulators (the two lanes of one f32x2 register pair when ZO_PACKED_SQ)
+// so consecutive additions do not wait on each other.  The thread's total
+// hi + lo is taken in binary64; the accumulated error is a few units of 2^-48
+// of the thread's sum.  Every operation is an explicit IEEE round-to-nearest
+// operation (a scalar _rn intrinsic, or an f32x2 instruction with .rn in
+// inline PTX), so nothing is contracted.  Tiles whose largest
 // |s| is 2^50 or more (squares near the binary32 overflow range, or inf/NaN),
 // or whose values are all nonzero and below 2^-40 (squares near underflow),
 // are summed in binary64 instead.  amax (the largest |s| bit pattern seen)
