@@ -42,6 +42,13 @@
 #ifndef ZO_PASS2_MIN_CTAS
 #define ZO_PASS2_MIN_CTAS 2
 #endif
+// With 16-bit masters a thread has fewer bytes in flight per tile (96 instead
+// of 112 with one gradient buffer), so pass 2 takes a third CTA per SM to keep
+// enough reads in flight (not with re-read buffers, whose eight loads in
+// flight need the registers of two).
+#ifndef ZO_PASS2_M16_MIN_CTAS
+#define ZO_PASS2_M16_MIN_CTAS 3
+#endif
 // The multi-buffer pass 1 holds eight 16-byte loads in flight per thread and
 // needs the larger register budget of three CTAs per SM.
 #ifndef ZO_MULTI_MIN_CTAS
@@ -795,7 +802,9 @@ __device__ __forceinline__ void f4_to(const float4& a, float* d) {
 // M16: low-precision master weights -- there is no fp32 master array; the
 // 16-bit parameter is widened, updated and stored back rounded.
 template <typename GT, typename PT, int SRC, bool M16>
-__global__ void __launch_bounds__(kThreads, ZO_PASS2_MIN_CTAS) pass2_kernel(const Pass2Args a) {
+__global__ void __launch_bounds__(kThreads, (M16 && SRC != 0) ? ZO_PASS2_M16_MIN_CTAS
+                                                               : ZO_PASS2_MIN_CTAS)
+    pass2_kernel(const Pass2Args a) {
   const Decision* dp = a.dec;
   if (dp->skip) return;
   Scalars c;
