@@ -634,6 +634,78 @@ def run_ours(args):
     return 0
 
 
+def run_zero2(args):
+    """The ZeRO-2 data-parallel step over the process group (Zero2Step with
+    the device kernels, NCCL): each rank holds its local gradients for the
+    whole model (N shards of the workload's size, K micro-steps), sends every
+    shard's bytes to its owner (all-to-all), steps its own shard and
+    all-gathers the 16-bit parameters.  Opt-in (--zero2); prints its own JSON
+    line with the whole model's params/s."""
+    import torch
+    import torch.distributed as dist
+
+    import synth
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    os.environ.setdefault("MASTER_PORT", "29511")
+    dist.init_process_group("nccl", rank=rank, world_size=ws, device_id=dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    import zero_sharded_mixed_05_gb300 as z
+    from zero_sharded_mixed_05_gb300.distributed import Zero2Step
+    w = WORKLOADS[args.workload]
+    if args.workload == "pertensor":
+        raise SystemExit("--zero2 applies to flat workloads")
+    S, K = w["numel"], w["K"]
+    psi = S * ws
+    code = z.FP16 if w["dtype"] == "fp16" else z.BF16
+    kind = synth.F16 if code == z.FP16 else synth.BF16
+    tdt = torch.float16 if code == z.FP16 else torch.bfloat16
+    cfg = z.make_config(numel=psi, world=ws, grad_dtype=code, lr=w["lr"], weight_decay=w["wd"],
+                        max_grad_norm=w["clip"], dynamic_scale=w["dynamic"],
+                        init_scale=w["scale"], scale_window=1000,
+                        master16=w.get("master16", False))
+    zs = Zero2Step(cfg, backend="device")
+    master = torch.empty(S, dtype=torch.float32, device=dev)
+    synth.fill_gpu(master, w["seed"], 0, rank * S, 0.02, synth.F32)
+    m, v = torch.zeros(S, device=dev), torch.zeros(S, device=dev)
+    p16 = torch.zeros(psi, dtype=tdt, device=dev)
+    p16[rank * S:(rank + 1) * S].copy_(master)
+    if w.get("master16"):
+        master = None
+    grads = []
+    for k in range(K):
+        g = torch.empty(psi, dtype=tdt, device=dev)
+        synth.fill_gpu(g, w["seed"], 1 + rank * K + k, 0, w["sigma"] * w["scale"], kind)
+        grads.append(g)
+    for _ in range(args.warmup):
+        zs.step(grads, master, m, v, p16)
+    dist.barrier()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        zs.step(grads, master, m, v, p16)
+    b.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    ms = max_over_ranks(a.elapsed_time(b) / args.steps, dev)
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC, "value": psi / (ms * 1e-3), "unit": "params/s", "impl": "zero2",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded SplitMix64 / Irwin-Hall), resident in HBM",
+            "config": {"workload": w["desc"] + " [ZeRO-2 across the ranks: all-to-all of the "
+                       "gradient bytes, step of the own shard, all-gather of the 16-bit "
+                       "parameters]", "params_per_gpu": S, "params_total": psi,
+                       "micro_steps": K, "parallelism": f"zero2-dp{ws}"}}))
+    zs.close()
+    dist.destroy_process_group()
+
+
 def run_offload(args):
     """The offloaded step (zero_host_step) of a flat workload on host buffers,
     run by CPU threads: params/s over `--steps` steps after `--warmup`."""
@@ -696,6 +768,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--numel", type=int, default=0,
                     help="override the flat workload's parameters per shard (profiling runs)")
+    ap.add_argument("--zero2", action="store_true",
+                    help="time the ZeRO-2 step with its collectives over the process group")
     ap.add_argument("--offload", action="store_true",
                     help="time the offloaded step (CPU threads, host buffers) instead")
     ap.add_argument("--threads", type=int, default=0,
@@ -714,6 +788,8 @@ def main():
         return run_reference(args)
     if args.offload:
         return run_offload(args)
+    if args.zero2:
+        return run_zero2(args)
     return run_ours(args)
 
 

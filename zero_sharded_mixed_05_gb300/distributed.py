@@ -100,8 +100,13 @@ class Zero2Step:
         if not param16.is_contiguous():
             raise ValueError("param16 must be contiguous (it is gathered in place)")
         S, r = self.S, self.rank
-        mine = param16[r * S:(r + 1) * S].clone()
-        dist.all_gather_into_tensor(_bytes(param16), _bytes(mine), group=self.group)
+        out = _bytes(param16)
+        if dist.get_backend(self.group) == "nccl":
+            # in place: the rank's own shard already sits at its offset
+            dist.all_gather_into_tensor(out, out[r * S * 2:(r + 1) * S * 2], group=self.group)
+        else:
+            mine = param16[r * S:(r + 1) * S].clone()
+            dist.all_gather_into_tensor(out, _bytes(mine), group=self.group)
 
     def step(self, grads, master, m, v, param16, stream=None):
         """Exchange, statistics, fold, step, all-gather; returns the step's
