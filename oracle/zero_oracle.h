@@ -15,7 +15,8 @@
  *   [AIQZ]  "DeepSpeed ZeRO引擎深入" (aiqz.cc): "显存四巨头", "ZeRO三阶段",
  *           "混合精度", "Python 演示" (the NumPy ZeROStage1 demo).
  *   [JWZ]   "LLM-train tutorials, ch01 项目背景与定位" (jwzheng96.github.io):
- *           §1.2, the M_DDP and M_ZeRO-1/2/3 equations and the stage table.
+ *           §1.2, the M_DDP and M_ZeRO-1/2/3 equations and the stage table;
+ *           §1.7, the list of later additions (low-precision master weights).
  *   [ALGO]  "DeepSpeed framework interview answer" (algomooc.com):
  *           "ZeRO 三阶段".
  *   [AIDH]  "DeepSpeed" (aidhplus.com): ZeRO-1/2/3 paragraphs, dynamic
@@ -29,6 +30,13 @@
  * -ffp-contract=off, never -ffast-math), computes per-step scalars in binary64
  * and rounds each once to binary32, and accumulates the squared-gradient sum
  * in binary64.
+ *
+ * Parity unpinned (readings of what the pages name without defining; each is
+ * pinned to its reading, not to the pages): the hysteresis rule of
+ * orc_decide (the scale falls on the hysteresis-th overflow since it last
+ * changed), the linear shape of WarmupLR in orc_decide (its endpoints and
+ * update counting are the pages'), and low-precision master weights in
+ * orc_update (master == NULL: the 16-bit copy is the master, [JWZ] §1.7).
  */
 #ifndef ZERO_ORACLE_H
 #define ZERO_ORACLE_H
