@@ -174,9 +174,12 @@ inline uint16_t f32_to_f16(float x) {
 }
 
 // ------------------------------------------------------------------ sums of squares
-// Compensated binary64 accumulation in four independent lanes (Knuth's
-// TwoSum on each addition): the lanes' error terms keep the sum of the exact
-// binary64 squares to far below binary64 precision.
+// Compensated binary64 accumulation in four independent lanes.  The square of
+// a binary32 value is exact in binary64; each lane adds groups of four squares
+// ((a^2 + b^2) + (c^2 + d^2), a few units of 2^-53 of the group) into its
+// (hi, lo) pair with Knuth's TwoSum, so the total stays within a few units of
+// 2^-53 of the exact sum of squares, like the device's.  Lane l takes every
+// fourth element, so the four lanes are the lanes of a vector.
 struct SqSum {
   double hi[4] = {0, 0, 0, 0}, lo[4] = {0, 0, 0, 0};
   static inline void two_sum(double& hi, double& lo, double x) {
@@ -185,11 +188,14 @@ struct SqSum {
     lo += (hi - (t - bp)) + (x - bp);
     hi = t;
   }
+  static inline double sq(float x) { return (double)x * (double)x; }
   void add_block(const float* s, int64_t n) {
     int64_t j = 0;
-    for (; j + 4 <= n; j += 4)
-      for (int l = 0; l < 4; ++l) two_sum(hi[l], lo[l], (double)s[j + l] * (double)s[j + l]);
-    for (; j < n; ++j) two_sum(hi[0], lo[0], (double)s[j] * (double)s[j]);
+    for (; j + 16 <= n; j += 16)
+      for (int l = 0; l < 4; ++l)  // lane l: elements j + l + 4k, k = 0..3
+        two_sum(hi[l], lo[l], (sq(s[j + l]) + sq(s[j + 4 + l])) +
+                                  (sq(s[j + 8 + l]) + sq(s[j + 12 + l])));
+    for (; j < n; ++j) two_sum(hi[0], lo[0], sq(s[j]));
   }
   // fold into (h, l) in lane order
   void into(double& h, double& l) const {
