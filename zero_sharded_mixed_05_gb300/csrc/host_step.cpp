@@ -175,8 +175,8 @@ inline uint16_t f32_to_f16(float x) {
 
 // ------------------------------------------------------------------ sums of squares
 // Compensated binary64 accumulation in four independent lanes.  The square of
-// a binary32 value is exact in binary64; each lane adds groups of four squares
-// ((a^2 + b^2) + (c^2 + d^2), a few units of 2^-53 of the group) into its
+// a binary32 value is exact in binary64; each lane adds groups of eight
+// squares (a pairwise sum, a few units of 2^-53 of the group) into its
 // (hi, lo) pair with Knuth's TwoSum, so the total stays within a few units of
 // 2^-53 of the exact sum of squares, like the device's.  Lane l takes every
 // fourth element, so the four lanes are the lanes of a vector.
@@ -191,10 +191,12 @@ struct SqSum {
   static inline double sq(float x) { return (double)x * (double)x; }
   void add_block(const float* s, int64_t n) {
     int64_t j = 0;
-    for (; j + 16 <= n; j += 16)
-      for (int l = 0; l < 4; ++l)  // lane l: elements j + l + 4k, k = 0..3
-        two_sum(hi[l], lo[l], (sq(s[j + l]) + sq(s[j + 4 + l])) +
-                                  (sq(s[j + 8 + l]) + sq(s[j + 12 + l])));
+    for (; j + 32 <= n; j += 32)
+      for (int l = 0; l < 4; ++l) {  // lane l: elements j + l + 4k, k = 0..7
+        const float* q = s + j + l;
+        two_sum(hi[l], lo[l], ((sq(q[0]) + sq(q[4])) + (sq(q[8]) + sq(q[12]))) +
+                                  ((sq(q[16]) + sq(q[20])) + (sq(q[24]) + sq(q[28]))));
+      }
     for (; j < n; ++j) two_sum(hi[0], lo[0], sq(s[j]));
   }
   // fold into (h, l) in lane order
