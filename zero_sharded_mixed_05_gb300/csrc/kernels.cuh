@@ -247,7 +247,8 @@ __device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
 
 struct SqAcc {
 #if ZO_PACKED_SQ
-  f32x2 H = 0ull, L = 0ull;  // lane 0 and lane 1 in one register each
+  f32x2 H = 0ull, L = 0ull;    // lane 0 and lane 1 in one register each
+  f32x2 H2 = 0ull, L2 = 0ull;  // a second pair (add_raw16_2): two dependency chains
 #else
   float hi0 = 0.0f, lo0 = 0.0f, hi1 = 0.0f, lo1 = 0.0f;
 #endif
@@ -292,8 +293,8 @@ struct SqAcc {
     two_sum_add(hi1, lo1, b);
 #endif
   }
-  __device__ __forceinline__ void pair_exact(float a, float b) {
 #if ZO_PACKED_SQ
+  static __device__ __forceinline__ void pair_exact_into(f32x2& H, f32x2& L, float a, float b) {
     const f32x2 X = f2_pack(a, b);
     const f32x2 P = f2_mul(X, X);
     const f32x2 T = f2_add(H, P);
@@ -301,6 +302,11 @@ struct SqAcc {
     const f32x2 AP = f2_sub(T, BP);
     L = f2_add(L, f2_add(f2_sub(H, AP), f2_sub(P, BP)));
     H = T;
+  }
+#endif
+  __device__ __forceinline__ void pair_exact(float a, float b) {
+#if ZO_PACKED_SQ
+    pair_exact_into(H, L, a, b);
 #else
     two_sum_add_exact(hi0, lo0, a);
     two_sum_add_exact(hi1, lo1, b);
@@ -358,6 +364,33 @@ struct SqAcc {
       slow = __dadd_rn(slow, d);
     }
   }
+#if ZO_PACKED_SQ
+  // As add_raw16 for two blocks of eight, into the two accumulator pairs.
+  template <typename GT>
+  __device__ __forceinline__ void add_raw16_2(const uint4& r, const uint4& q) {
+    const uint32_t m0 = __vmaxu2(__vmaxu2(r.x & 0x7fff7fffu, r.y & 0x7fff7fffu),
+                                 __vmaxu2(r.z & 0x7fff7fffu, r.w & 0x7fff7fffu));
+    const uint32_t m1 = __vmaxu2(__vmaxu2(q.x & 0x7fff7fffu, q.y & 0x7fff7fffu),
+                                 __vmaxu2(q.z & 0x7fff7fffu, q.w & 0x7fff7fffu));
+    const uint32_t mm = __vmaxu2(m0, m1);
+    const uint32_t t16 = max(mm & 0xffffu, mm >> 16);
+    amax16 = max(amax16, t16);
+    if (Fmt<GT>::fast16(t16)) {
+      const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+      const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 x = Fmt<GT>::dec2(w[k]);
+        const float2 y = Fmt<GT>::dec2(u[k]);
+        pair_exact_into(H, L, x.x, x.y);
+        pair_exact_into(H2, L2, y.x, y.y);
+      }
+    } else {
+      add_raw16<GT>(r);
+      add_raw16<GT>(q);
+    }
+  }
+#endif
   template <typename GT>
   __device__ __forceinline__ bool overflowed() const {
     return amax >= 0x7f800000u || amax16 >= Fmt<GT>::kInf;
@@ -367,8 +400,12 @@ struct SqAcc {
 #if ZO_PACKED_SQ
     const float hi0 = f2_lo(H), lo0 = f2_lo(L), hi1 = f2_hi(H), lo1 = f2_hi(L);
 #endif
-    const double a = __dadd_rn((double)hi0, (double)lo0);
-    const double b = __dadd_rn((double)hi1, (double)lo1);
+    double a = __dadd_rn((double)hi0, (double)lo0);
+    double b = __dadd_rn((double)hi1, (double)lo1);
+#if ZO_PACKED_SQ
+    a = __dadd_rn(a, __dadd_rn((double)f2_lo(H2), (double)f2_lo(L2)));
+    b = __dadd_rn(b, __dadd_rn((double)f2_hi(H2), (double)f2_hi(L2)));
+#endif
     return __dadd_rn(__dadd_rn(a, b), slow);
   }
 };
@@ -690,8 +727,20 @@ __global__ void __launch_bounds__(kThreads, bulk_min_ctas(CT))
     if (!s_err) {
       if (whole(cur, t0)) {
         const uint4* sb = &stage_buf[(i % S) * kChunkTiles * kThreads + tid];
+#if ZO_PACKED_SQ
+        if constexpr (CT >= 8) {
+          // the 3-CTA/SM build has the registers for two accumulator chains
+#pragma unroll
+          for (int k = 0; k < kChunkTiles; k += 2)
+            acc.add_raw16_2<GT>(sb[k * kThreads], sb[(k + 1) * kThreads]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < kChunkTiles; ++k) acc.add_raw16<GT>(sb[k * kThreads]);
+        }
+#else
 #pragma unroll
         for (int k = 0; k < kChunkTiles; ++k) acc.add_raw16<GT>(sb[k * kThreads]);
+#endif
       } else {
         for (int k = 0; k < kChunkTiles; ++k) {
           const int64_t tile = t0 + k;
