@@ -665,7 +665,8 @@ constexpr int bulk_min_ctas(int chunk_tiles) { return chunk_tiles >= 8 ? 3 : ZO_
 
 // Single gradient buffer, staged through shared memory by bulk copies.  The
 // work unit is a chunk of CT consecutive tiles (each thread reduces 8*CT
-// elements per chunk); thread 0 keeps ZO_BULK_STAGES chunks in flight per CTA
+// elements per chunk, in two independent TwoSum chains that take the tiles
+// in turn); thread 0 keeps ZO_BULK_STAGES chunks in flight per CTA
 // with one cp.async.bulk of CT * 4 KiB each, so the reducing threads read
 // shared memory instead of waiting on global loads.  Chunks of 4 tiles at 4
 // CTAs per SM balance short shards best; chunks of 8 tiles at 3 CTAs per SM
@@ -681,6 +682,7 @@ __global__ void __launch_bounds__(kThreads, bulk_min_ctas(CT))
   constexpr int kChunkTiles = CT;
   extern __shared__ __align__(128) uint4 stage_buf[];  // [S][CT][kThreads]
   __shared__ __align__(8) unsigned long long bar[S];
+  __shared__ int s_whole[S];  // 1: the stage holds its chunk (copied whole)
   __shared__ double red[kThreads / 32];
   __shared__ int s_last, s_err;
   const int tid = threadIdx.x;
@@ -689,21 +691,22 @@ __global__ void __launch_bounds__(kThreads, bulk_min_ctas(CT))
   const int64_t mine = (int64_t)blockIdx.x < G && nchunks > (int64_t)blockIdx.x
                            ? (nchunks - 1 - blockIdx.x) / G + 1
                            : 0;
-  // a chunk is copied whole when its four tiles are full tiles of one vector run
-  auto whole = [&](RunCursorLite& c, int64_t t0) -> bool {
-    c.seek(a.segs, a.nseg, t0);
-    return c.s.vec && t0 + kChunkTiles <= c.end &&
-           (t0 + kChunkTiles - c.s.tile0) * kTile <= c.s.n;
-  };
-  RunCursorLite pcur;  // thread 0's cursor for issuing copies
+  // Thread 0 looks each chunk up (a fresh cursor, so no run state stays live
+  // across the loop) and tells the others through s_whole whether the chunk
+  // was copied: it is when its tiles are full tiles of one vector run.
   auto issue = [&](int64_t i) {
     const int64_t t0 = (blockIdx.x + i * G) * kChunkTiles;
     unsigned long long* b = &bar[i % S];
     if (a.inject_wait_fault && blockIdx.x == 0 && i == 0) return;  // test hook
-    if (whole(pcur, t0)) {
+    RunCursorLite c;
+    c.seek(a.segs, a.nseg, t0);
+    const bool whole = c.s.vec && t0 + kChunkTiles <= c.end &&
+                       (t0 + kChunkTiles - c.s.tile0) * kTile <= c.s.n;
+    s_whole[i % S] = whole ? 1 : 0;
+    if (whole) {
       mbar_arrive_expect_tx(b, kChunkTiles * kTile * 2);
       bulk_load(&stage_buf[(i % S) * kChunkTiles * kThreads],
-                grad_ptr(a.gptrs, pcur.s, 0) + (t0 - pcur.s.tile0) * kTile,
+                grad_ptr(a.gptrs, c.s, 0) + (t0 - c.s.tile0) * kTile,
                 kChunkTiles * kTile * 2, b);
     } else {
       mbar_arrive(b);
@@ -719,29 +722,24 @@ __global__ void __launch_bounds__(kThreads, bulk_min_ctas(CT))
   if (tid == 0)
     for (int64_t i = 0; i < mine && i < S; ++i) issue(i);
   SqAcc acc;
-  RunCursorLite cur;
   int64_t issued = mine < S ? mine : S;
   for (int64_t i = 0; i < mine; ++i) {
     if (!mbar_wait_bounded(&bar[i % S], (uint32_t)((i / S) & 1))) s_err = 1;
     const int64_t t0 = (blockIdx.x + i * G) * kChunkTiles;
     if (!s_err) {
-      if (whole(cur, t0)) {
+      if (*reinterpret_cast<volatile int*>(&s_whole[i % S])) {
         const uint4* sb = &stage_buf[(i % S) * kChunkTiles * kThreads + tid];
 #if ZO_PACKED_SQ
-        if constexpr (CT >= 8) {
-          // the 3-CTA/SM build has the registers for two accumulator chains
+        // tiles in pairs, into two accumulator chains (CT is even)
 #pragma unroll
-          for (int k = 0; k < kChunkTiles; k += 2)
-            acc.add_raw16_2<GT>(sb[k * kThreads], sb[(k + 1) * kThreads]);
-        } else {
-#pragma unroll
-          for (int k = 0; k < kChunkTiles; ++k) acc.add_raw16<GT>(sb[k * kThreads]);
-        }
+        for (int k = 0; k < kChunkTiles; k += 2)
+          acc.add_raw16_2<GT>(sb[k * kThreads], sb[(k + 1) * kThreads]);
 #else
 #pragma unroll
         for (int k = 0; k < kChunkTiles; ++k) acc.add_raw16<GT>(sb[k * kThreads]);
 #endif
       } else {
+        RunCursorLite cur;
         for (int k = 0; k < kChunkTiles; ++k) {
           const int64_t tile = t0 + k;
           if (tile >= a.ntiles) break;
