@@ -261,6 +261,11 @@ zero_status zero_opt_fold_stats(const zero_opt_stats* per_rank, int32_t n,
  * update's learning rate (lr, or the WarmupLR value) and after scale_window
  * consecutive applied steps the scale is multiplied by scale_factor
  * ("DeepSpeed tutorial" §2.2, §2.4, §3.2).
+ * The first call with a given set of buffers builds and uploads a small run
+ * table (one cudaMalloc, cached by content).  After that, a call makes no
+ * allocation and no host synchronization; it only launches kernels on `stream`,
+ * and the decision stays on the device.  Such a call can therefore be captured
+ * into a CUDA graph (stream capture) and the graph replayed once per step.
  * Errors: EINVAL (h/bufs/grads NULL, a NULL state or gradient pointer for a
  * non-empty shard, R or K < 1, R*K > 1024), ERANGE (rank outside [0, world)),
  * ECUDA (no device, wrong current device, or a launch failure). */
