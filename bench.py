@@ -527,7 +527,7 @@ def run_ours(args):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     for trio in evs:
         for e in trio:
-            e.record(stream)
+            e.record(stream)   # every event has a recorded state before the region
     torch.cuda.synchronize()
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
@@ -539,14 +539,23 @@ def run_ours(args):
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    # Per-pass CUDA events (the timing hook) on every EVERY-th timed step.  An
+    # event recorded between the two passes turns pass 2's programmatic
+    # dependent launch into an ordinary one, so the other steps run exactly
+    # as a caller runs them.
+    EVERY = 8
+    sampled = list(range(0, K, EVERY))
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0 = time.time()
     start.record(stream)
     for i in range(K):
-        z.zero_opt_set_events(setup.h, *evs[i])
-        setup.step(sp)
+        if i % EVERY == 0:
+            z.zero_opt_set_events(setup.h, *evs[i])
+            setup.step(sp)
+            z.zero_opt_set_events(setup.h)
+        else:
+            setup.step(sp)
     end.record(stream)
-    z.zero_opt_set_events(setup.h)
     torch.cuda.synchronize()
     t1 = time.time()
     launches = z.zero_opt_launch_count(setup.h) - launches0
@@ -556,8 +565,8 @@ def run_ours(args):
     # keep sampling a little after the region, then stop
     clocks.stop()
     clk = clocks.summary(t0, t1)
-    p1 = [evs[i][0].elapsed_time(evs[i][1]) for i in range(K)]
-    p2 = [evs[i][1].elapsed_time(evs[i][2]) for i in range(K)]
+    p1 = [evs[i][0].elapsed_time(evs[i][1]) for i in sampled]
+    p2 = [evs[i][1].elapsed_time(evs[i][2]) for i in sampled]
     if ws > 1:
         ms_total = max_over_ranks(ms_total, dev)
     ms_step = ms_total / K
@@ -616,7 +625,10 @@ def run_ours(args):
                          "frac": achieved / peak, "peak_source": peak_src + " (hbm_gbs)",
                          "traffic": traffic, "traffic_source": traffic_src,
                          "bytes_per_launch": p2_bytes,
-                         "avg_launch_ms": p2_ms, "pass1_avg_ms": p1_ms},
+                         "avg_launch_ms": p2_ms, "pass1_avg_ms": p1_ms,
+                         "launches_timed": len(sampled),
+                         "timing": "CUDA events around each pass on every %d-th timed "
+                                   "step" % EVERY},
             "e2e": {"value": e2e_value, "unit": "params/s",
                     "h2d_bytes_per_step": setup.input_bytes(),
                     "d2h_bytes_per_step": setup.output_bytes(), "ms_per_step": e2e_ms,

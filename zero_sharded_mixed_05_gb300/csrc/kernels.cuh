@@ -193,6 +193,27 @@ __device__ __forceinline__ const unsigned short* grad_ptr(const void* const* gpt
   return reinterpret_cast<const unsigned short*>(raw);
 }
 
+// Programmatic dependent launch: pass 1 lets pass 2 be scheduled before it
+// ends (each CTA signals at its start); pass 2 waits for pass 1 to complete,
+// with all its memory visible, before it reads anything pass 1 writes.
+#ifndef ZO_PDL
+#define ZO_PDL 1
+#endif
+__device__ __forceinline__ void pdl_launch_dependents() {
+#if ZO_PDL
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+}
+__device__ __forceinline__ void pdl_wait() {
+#if ZO_PDL
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+}
+// Warm L2 with `bytes` at `p` (16-byte aligned, a multiple of 16 bytes).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ------------------------------------------------------------- sum of squares
 // The global norm needs the sum of squares of the reduced gradients to well
 // below binary32 precision (the clip coefficient is rounded to binary32 from
@@ -551,6 +572,7 @@ __device__ __noinline__ Sums8 pass1_elementwise_sums(const Pass1Args& a, int64_t
 template <typename GT>
 __global__ void __launch_bounds__(kThreads, ZO_PASS1_MIN_CTAS)
     pass1_single_kernel(const Pass1Args a) {
+  pdl_launch_dependents();
   __shared__ double red[kThreads / 32];
   __shared__ int s_last;
   constexpr int U = ZO_PASS1_UNROLL;
@@ -678,6 +700,7 @@ constexpr int bulk_min_ctas(int chunk_tiles) { return chunk_tiles >= 8 ? 3 : ZO_
 template <typename GT, int CT>
 __global__ void __launch_bounds__(kThreads, bulk_min_ctas(CT))
     pass1_bulk_kernel(const Pass1Args a) {
+  pdl_launch_dependents();
   constexpr int S = ZO_BULK_STAGES;
   constexpr int kChunkTiles = CT;
   extern __shared__ __align__(128) uint4 stage_buf[];  // [S][CT][kThreads]
@@ -779,6 +802,7 @@ __global__ void __launch_bounds__(kThreads, bulk_min_ctas(CT))
 template <typename GT, bool STASH>
 __global__ void __launch_bounds__(kThreads, ZO_MULTI_MIN_CTAS)
     pass1_multi_kernel(const Pass1Args a) {
+  pdl_launch_dependents();
   __shared__ double red[kThreads / 32];
   __shared__ int s_last;
   const int tid = threadIdx.x;
@@ -852,6 +876,24 @@ template <typename GT, typename PT, int SRC, bool M16>
 __global__ void __launch_bounds__(kThreads, (M16 && SRC != 0) ? ZO_PASS2_M16_MIN_CTAS
                                                                : ZO_PASS2_MIN_CTAS)
     pass2_kernel(const Pass2Args a) {
+  const int64_t G0 = gridDim.x;
+  if (threadIdx.x == 0 && (int64_t)blockIdx.x < a.ntiles) {
+    // Before the wait this overlaps the end of pass 1, so only data pass 1
+    // never writes is touched: warm L2 with the state (and a single gradient
+    // buffer) of this CTA's first tile, when it is a full 16-byte aligned one.
+    const int64_t first = blockIdx.x + (a.ntiles - 1 - blockIdx.x) / G0 * G0;
+    RunCursor c;
+    c.seek(a.segs, a.nseg, first);
+    const int64_t base = (first - c.s.tile0) * kTile;
+    if (c.s.vec && base + kTile <= c.s.n) {
+      if (!M16) prefetch_l2(c.s.master + base, kTile * 4);
+      prefetch_l2(c.s.m + base, kTile * 4);
+      prefetch_l2(c.s.v + base, kTile * 4);
+      if (M16) prefetch_l2(static_cast<const unsigned short*>(c.s.p16) + base, kTile * 2);
+      if (SRC == 1) prefetch_l2(grad_ptr(a.gptrs, c.s, 0) + base, kTile * 2);
+    }
+  }
+  pdl_wait();
   const Decision* dp = a.dec;
   if (dp->skip) return;
   Scalars c;

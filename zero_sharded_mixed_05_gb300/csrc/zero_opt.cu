@@ -352,12 +352,27 @@ Pass2Fn pick_pass2(int gdt, int pdt, int src, bool m16) {
 }
 
 
+// `dependent`: launched as a programmatic dependent of the previous kernel on
+// the stream (pass 2 after pass 1): it may start while that kernel ends and
+// waits for its completion itself (griddepcontrol.wait) before using results.
 zero_status launch_kernel(zero_opt_t h, const void* fn, int grid, void* args,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, bool dependent = false) {
   void* params[] = {args};
-  cudaError_t e = cudaLaunchKernel(fn, dim3(grid), dim3(zo::kThreads), params, dyn_smem(fn),
-                                   stream);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernel");
+  cudaLaunchConfig_t lc;
+  std::memset(&lc, 0, sizeof(lc));
+  lc.gridDim = dim3(grid);
+  lc.blockDim = dim3(zo::kThreads);
+  lc.dynamicSmemBytes = dyn_smem(fn);
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (dependent && ZO_PDL) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+  }
+  cudaError_t e = cudaLaunchKernelExC(&lc, fn, params);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernelExC");
   h->launches += 1;
   return ZERO_OK;
 }
@@ -432,7 +447,9 @@ zero_status run(zero_opt_t h, int32_t rank, const std::vector<HostRun>& runs, in
       pick_pass2(h->cfg.grad_dtype, h->cfg.param_dtype, src, h->cfg.master16 != 0));
   int64_t g2 = (int64_t)occupancy(h, f2) * h->sms;
   g2 = std::min<int64_t>(g2, plan->ntiles);
-  st = launch_kernel(h, f2, (int)g2, &a2, stream);
+  // with the timing hook an event sits between the passes, and pass 2 is
+  // an ordinary launch
+  st = launch_kernel(h, f2, (int)g2, &a2, stream, h->ev[1] == nullptr);
   if (h->ev[2]) cudaEventRecord(h->ev[2], stream);
   return st;
 }
