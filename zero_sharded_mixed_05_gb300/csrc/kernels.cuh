@@ -1,16 +1,23 @@
 // kernels.cuh -- sm_103a kernels of the per-shard mixed-precision ZeRO step.
 //
-// pass1_single_kernel / pass1_multi_kernel (steps a1..a4): each CTA walks its
-//   tiles of the shard, sums the R*K 16-bit gradient buffers per element in
-//   binary32 (rank-major order, starting from +0; one buffer or many),
-//   optionally stores the sums (the stash), and accumulates
-//   the overflow flag and the sum of squares.  CTAs publish one partial each;
-//   the CTA that finishes last (atomic ticket, no waiting) folds the partials
-//   in CTA order in binary64, takes the per-step decisions (skip, clip
-//   coefficient, Adam scalars) and advances the rank's loss-scaler state.
-// pass2_kernel (steps a5..a7): reads the decision; on a skip every CTA returns
-//   at once; otherwise it applies unscale x clip, AdamW on the fp32 master
-//   copy and m, v, and writes the 16-bit parameter copy.
+// Pass 1 (steps a1..a4) has three forms:
+//   pass1_bulk_kernel (one gradient buffer, the usual case): chunks of 4 or 8
+//     tiles are staged into shared memory by bulk copies (TMA, cp.async.bulk
+//     on an mbarrier, two stages per CTA);
+//   pass1_multi_kernel (R*K > 1 buffers): summed per element in binary32
+//     (rank-major order, starting from +0), optionally stored (the stash);
+//   pass1_single_kernel: the one-buffer form without bulk copies (built when
+//     ZO_PASS1_BULK is 0).
+//   Each accumulates the overflow flag and the exact sum of squares.  CTAs
+//   publish one partial each; the CTA that finishes last (atomic ticket, no
+//   waiting) folds the partials in CTA order in binary64, takes the per-step
+//   decisions (skip, clip coefficient, Adam scalars) and advances the rank's
+//   loss-scaler state.  One extra CTA computes the next step's binary64
+//   scalars while the others stream.
+// pass2_kernel (steps a5..a7): a programmatic dependent launch of pass 1; it
+//   reads the decision, and on a skip every CTA returns at once; otherwise it
+//   applies unscale x clip, AdamW on the fp32 master copy (or the widened
+//   16-bit master) and m, v, and writes the 16-bit parameter copy.
 //
 // Both passes are HBM-bandwidth bound streaming kernels.  Tiles are 2048
 // elements (256 threads x 8); a thread moves each of its streams with one
