@@ -463,6 +463,15 @@ zero_status zero_host_grad_stats(zero_host_t h, int32_t rank, const zero_opt_buf
                                  zero_opt_stats* out);
 zero_status zero_host_step(zero_host_t h, int32_t rank, const zero_opt_buffers* bufs,
                            const zero_opt_stats* global);
+/* The per-tensor list forms, as zero_opt_grad_stats_tensors and
+ * zero_opt_step_tensors with host pointers: the statistics are those of the
+ * concatenation in list order, and every tensor is updated with the one
+ * decision.  The threads split the list by blocks of 1024 elements across
+ * tensors.  Errors: as the device forms, with no ECUDA. */
+zero_status zero_host_grad_stats_tensors(zero_host_t h, int32_t rank,
+                                         const zero_opt_tensor_list* list, zero_opt_stats* out);
+zero_status zero_host_step_tensors(zero_host_t h, int32_t rank, const zero_opt_tensor_list* list,
+                                   const zero_opt_stats* global);
 zero_status zero_host_loss_scale(zero_host_t h, int32_t rank, zero_opt_scaler_state* out);
 zero_status zero_host_set_loss_scale(zero_host_t h, int32_t rank,
                                      const zero_opt_scaler_state* state);

@@ -207,3 +207,65 @@ def test_low_precision_master(z, orc, pdtype):
     run_host(z, orc, numel=60_001, world=2, R=2, gdtype=O.BF16, pdtype=pdtype, steps=5,
              threads=3, lr=1e-3, wd=0.01, max_norm=0.5, sigma=1e-2, dynamic=True,
              init_scale=4.0, inject={3: [(1, 4242, 0x7F80)]}, master16=True)
+
+
+@pytest.mark.parametrize("threads,master16", [(1, False), (5, False), (3, True)])
+def test_tensor_list(z, orc, threads, master16):
+    """zero_host_step_tensors on a list of ragged tensors (R*K = 2*2 fp16
+    buffers, clipping): the statistics of the concatenation, every tensor
+    updated with the one decision, bit-identical to the oracle; an overflow in
+    the last tensor at step 2 skips the step for all of them."""
+    sizes = [5000, 1, 3000, 1024, 77_777, 0, 2049]
+    R, K, steps = 2, 2, 4
+    cfg = z.make_config(numel=sum(sizes), world=1, grad_dtype=O.FP16, lr=1e-3,
+                        weight_decay=0.01, max_grad_norm=0.4, dynamic_scale=True,
+                        init_scale=8.0, master16=master16)
+    hp = O.hparams(lr=1e-3, weight_decay=0.01, max_grad_norm=0.4, dynamic_scale=True,
+                   scale_window=1000)
+    h = z.zero_host_create(cfg, threads)
+    total = sum(sizes)
+    offs = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    p0 = synth.normal_np(0x5EED0501, 0, 0, total, 0.02, synth.F32)
+    q0 = orc.f32_to_16(p0, O.FP16)
+    mine, ref = [], []
+    for i, n in enumerate(sizes):
+        o = offs[i]
+        mine.append(dict(master=None if master16 else p0[o:o + n].copy(),
+                         m=np.zeros(n, np.float32), v=np.zeros(n, np.float32),
+                         p16=q0[o:o + n].copy() if master16 else np.zeros(n, np.uint16)))
+        ref.append([None if master16 else p0[o:o + n].copy(), np.zeros(n, np.float32),
+                    np.zeros(n, np.float32),
+                    q0[o:o + n].copy() if master16 else np.zeros(n, np.uint16)])
+    sc = O.scaler(8.0)
+    skips = []
+    for step in range(1, steps + 1):
+        flat = [synth.normal_np(0x5EED0501, 1 + b, step * total, total, 1e-3 * sc.scale,
+                                synth.F16) for b in range(R * K)]
+        if step == 2:
+            flat[3][offs[-2] + 7] = 0x7C00
+        items = [dict(numel=n, master=mine[i]["master"], m=mine[i]["m"], v=mine[i]["v"],
+                      param16=mine[i]["p16"],
+                      grads=[fb[offs[i]:offs[i] + n] for fb in flat]) for i, n in enumerate(sizes)]
+        lst = z.make_tensor_list(items, n_ranks=R, n_micro=K)
+        st = z.zero_host_grad_stats_tensors(h, 0, lst)
+        z.zero_host_step_tensors(h, 0, lst)
+        info = z.zero_host_last_step(h)
+        s_all = orc.reduce(flat, O.FP16)
+        G = orc.stats_of(s_all)
+        d = orc.decide(hp, sc, G, float(R * K))
+        for i, n in enumerate(sizes):
+            o = offs[i]
+            orc.update(d, s_all[o:o + n].copy(), *ref[i], O.FP16)
+        assert info.skipped == d.skip and st.nonfinite == G.nonfinite
+        if not d.skip:
+            assert info.coef == d.coef
+        skips.append(d.skip)
+        for i in range(len(sizes)):
+            if not master16:
+                assert (mine[i]["master"].view(np.uint32) == ref[i][0].view(np.uint32)).all()
+            assert (mine[i]["m"].view(np.uint32) == ref[i][1].view(np.uint32)).all()
+            assert (mine[i]["v"].view(np.uint32) == ref[i][2].view(np.uint32)).all()
+            assert (mine[i]["p16"] == ref[i][3]).all()
+    assert skips == [0, 1, 0, 0]
+    assert z.zero_host_loss_scale(h, 0).as_tuple() == sc.as_tuple()
+    z.zero_host_destroy(h)

@@ -124,6 +124,9 @@ SIGNATURES = [
     ("zero_host_threads", _i32, [_vp, _P(_i32)]),
     ("zero_host_grad_stats", _i32, [_vp, _i32, _P(zero_opt_buffers), _P(zero_opt_stats)]),
     ("zero_host_step", _i32, [_vp, _i32, _P(zero_opt_buffers), _P(zero_opt_stats)]),
+    ("zero_host_grad_stats_tensors", _i32,
+     [_vp, _i32, _P(zero_opt_tensor_list), _P(zero_opt_stats)]),
+    ("zero_host_step_tensors", _i32, [_vp, _i32, _P(zero_opt_tensor_list), _P(zero_opt_stats)]),
     ("zero_host_loss_scale", _i32, [_vp, _i32, _P(zero_opt_scaler_state)]),
     ("zero_host_set_loss_scale", _i32, [_vp, _i32, _P(zero_opt_scaler_state)]),
     ("zero_host_last_step", _i32, [_vp, _P(zero_opt_step_info)]),
@@ -498,6 +501,18 @@ def zero_host_grad_stats(h, rank: int, bufs: zero_opt_buffers) -> zero_opt_stats
 def zero_host_step(h, rank: int, bufs: zero_opt_buffers, global_stats=None) -> None:
     gs = ctypes.byref(global_stats) if global_stats is not None else None
     _check(lib().zero_host_step(h, rank, ctypes.byref(bufs), gs), "zero_host_step")
+
+
+def zero_host_grad_stats_tensors(h, rank: int, lst: zero_opt_tensor_list) -> zero_opt_stats:
+    out = zero_opt_stats()
+    _check(lib().zero_host_grad_stats_tensors(h, rank, ctypes.byref(lst), ctypes.byref(out)),
+           "zero_host_grad_stats_tensors")
+    return out
+
+
+def zero_host_step_tensors(h, rank: int, lst: zero_opt_tensor_list, global_stats=None) -> None:
+    gs = ctypes.byref(global_stats) if global_stats is not None else None
+    _check(lib().zero_host_step_tensors(h, rank, ctypes.byref(lst), gs), "zero_host_step_tensors")
 
 
 def zero_host_loss_scale(h, rank: int) -> zero_opt_scaler_state:

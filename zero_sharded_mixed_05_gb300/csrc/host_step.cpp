@@ -209,15 +209,31 @@ struct SqSum {
 };
 
 // ------------------------------------------------------------------ the step
+// One run of elements with its own buffers: a flat shard, or one tensor of a
+// per-tensor list.
 struct Job {
   const zero_opt_config* cfg;
-  const uint16_t* const* g;  // per buffer: first element of the shard
+  const uint16_t* const* g;  // per buffer: first element of the run
   int nbuf;
-  int64_t n;                 // real elements of the shard
+  int64_t n;                 // elements of the run
   float* master;
   float* m;
   float* v;
-  uint16_t* p16;             // first element of the shard
+  uint16_t* p16;             // first element of the run
+};
+
+// The runs of a step and their blocks numbered across runs (run k's blocks
+// are first[k] .. first[k + 1] - 1), so that threads split the whole step by
+// block, whatever the run sizes.
+struct Work {
+  std::vector<Job> jobs;
+  std::vector<int64_t> first;  // jobs.size() + 1 entries
+  std::vector<const uint16_t*> gptrs;  // storage of every job's gradient pointers
+  void number_blocks() {
+    first.assign(1, 0);
+    for (const Job& j : jobs) first.push_back(first.back() + (j.n + kBlock - 1) / kBlock);
+  }
+  int64_t blocks() const { return first.back(); }
 };
 
 // Reduced binary32 sums of elements [j0, j0 + len) in buffer order.
@@ -235,11 +251,24 @@ inline void reduce_block(const Job& jb, int64_t j0, int64_t len, float* s) {
   }
 }
 
-void range_of(const Job& jb, int nt, int i, int64_t* lo, int64_t* hi) {
-  const int64_t blocks = (jb.n + kBlock - 1) / kBlock;
-  const int64_t per = (blocks + nt - 1) / nt;
-  *lo = std::min(jb.n, (int64_t)i * per * kBlock);
-  *hi = std::min(jb.n, (int64_t)(i + 1) * per * kBlock);
+// Thread i of nt: calls f(job, lo, hi) for the element ranges of its
+// contiguous share of the step's blocks, in block order.
+template <typename F>
+void for_share(const Work& w, int nt, int i, F&& f) {
+  const int64_t per = (w.blocks() + nt - 1) / nt;
+  const int64_t b0 = std::min(w.blocks(), (int64_t)i * per);
+  const int64_t b1 = std::min(w.blocks(), (int64_t)(i + 1) * per);
+  if (b0 >= b1) return;
+  size_t k = (size_t)(std::upper_bound(w.first.begin(), w.first.end(), b0) - w.first.begin()) - 1;
+  for (int64_t b = b0; b < b1; ++k) {
+    const int64_t end = std::min(b1, w.first[k + 1]);
+    if (end > b) {
+      const Job& jb = w.jobs[k];
+      const int64_t lo = (b - w.first[k]) * kBlock;
+      f(jb, lo, std::min(jb.n, (end - w.first[k]) * kBlock));
+      b = end;
+    }
+  }
 }
 
 struct Partial {
@@ -248,18 +277,16 @@ struct Partial {
   char pad[64 - 2 * sizeof(double) - sizeof(int)];
 };
 
-void stats_range(const Job& jb, int64_t lo, int64_t hi, Partial* out) {
+void stats_range(const Job& jb, int64_t lo, int64_t hi, SqSum* acc, int* bad) {
   alignas(64) float s[kBlock];
-  SqSum acc;
-  int bad = 0;
   for (int64_t j0 = lo; j0 < hi; j0 += kBlock) {
     const int64_t len = std::min(kBlock, hi - j0);
     reduce_block(jb, j0, len, s);
-    for (int64_t k = 0; k < len; ++k) bad |= !(std::fabs(s[k]) <= 3.40282347e38f);
-    acc.add_block(s, len);
+    int b = 0;
+    for (int64_t k = 0; k < len; ++k) b |= !(std::fabs(s[k]) <= 3.40282347e38f);
+    *bad |= b;
+    acc->add_block(s, len);
   }
-  acc.into(out->hi, out->lo);
-  out->nonfinite = bad;
 }
 
 void update_range(const Job& jb, const zo::Decision& d, int64_t lo, int64_t hi) {
@@ -323,9 +350,9 @@ zero_status check_rank(zero_host_t h, int32_t rank) {
   return ZERO_OK;
 }
 
-// Validate `b` and describe the rank's shard as a Job.
-zero_status make_job(zero_host_t h, int32_t rank, const zero_opt_buffers* b, bool need_state,
-                     std::vector<const uint16_t*>* g, Job* jb) {
+// Validate `b` and describe the rank's shard as a one-run Work.
+zero_status flat_work(zero_host_t h, int32_t rank, const zero_opt_buffers* b, bool need_state,
+                      Work* w) {
   zero_status st = check_rank(h, rank);
   if (st != ZERO_OK) return st;
   if (!b) return fail(ZERO_EINVAL, "buffers is NULL");
@@ -342,29 +369,78 @@ zero_status make_job(zero_host_t h, int32_t rank, const zero_opt_buffers* b, boo
     if (need_state && ((!h->cfg.master16 && !b->master) || !b->m || !b->v || !b->param16))
       return fail(ZERO_EINVAL, "master (unless master16), m, v and param16 must not be NULL");
   }
-  g->resize((size_t)nbuf);
+  w->gptrs.resize((size_t)nbuf);
   const int64_t goff = b->grads_shard_local ? 0 : begin;
   for (int64_t k = 0; k < nbuf; ++k)
-    (*g)[k] = b->grads[k] ? static_cast<const uint16_t*>(b->grads[k]) + goff : nullptr;
-  jb->cfg = &h->cfg;
-  jb->g = g->data();
-  jb->nbuf = (int)nbuf;
-  jb->n = real;
-  jb->master = h->cfg.master16 ? nullptr : b->master;
-  jb->m = b->m;
-  jb->v = b->v;
-  jb->p16 = b->param16 ? static_cast<uint16_t*>(b->param16) + (b->param16_shard_local ? 0 : begin)
-                       : nullptr;
+    w->gptrs[(size_t)k] = b->grads[k] ? static_cast<const uint16_t*>(b->grads[k]) + goff : nullptr;
+  Job jb;
+  jb.cfg = &h->cfg;
+  jb.g = w->gptrs.data();
+  jb.nbuf = (int)nbuf;
+  jb.n = real;
+  jb.master = h->cfg.master16 ? nullptr : b->master;
+  jb.m = b->m;
+  jb.v = b->v;
+  jb.p16 = b->param16 ? static_cast<uint16_t*>(b->param16) + (b->param16_shard_local ? 0 : begin)
+                      : nullptr;
+  w->jobs.assign(1, jb);
+  w->number_blocks();
   return ZERO_OK;
 }
 
-zero_opt_stats shard_stats(zero_host_t h, const Job& jb) {
+// Validate a per-tensor list and describe it as a Work of one run per tensor.
+zero_status list_work(zero_host_t h, int32_t rank, const zero_opt_tensor_list* l,
+                      bool need_state, Work* w) {
+  zero_status st = check_rank(h, rank);
+  if (st != ZERO_OK) return st;
+  if (!l) return fail(ZERO_EINVAL, "tensor list is NULL");
+  if (l->n_tensors < 0) return fail(ZERO_EINVAL, "n_tensors must be >= 0");
+  if (l->n_tensors > 0 && !l->tensors) return fail(ZERO_EINVAL, "tensors is NULL");
+  if (l->n_ranks < 1 || l->n_micro < 1) return fail(ZERO_EINVAL, "n_ranks and n_micro must be >= 1");
+  const int64_t nbuf = (int64_t)l->n_ranks * l->n_micro;
+  if (nbuf > zo::kMaxBufs)
+    return fail(ZERO_ERANGE, "n_ranks*n_micro = %lld exceeds %d", (long long)nbuf, zo::kMaxBufs);
+  w->gptrs.assign((size_t)(nbuf * l->n_tensors), nullptr);
+  w->jobs.clear();
+  for (int i = 0; i < l->n_tensors; ++i) {
+    const zero_opt_tensor& t = l->tensors[i];
+    if (t.numel < 0) return fail(ZERO_EINVAL, "tensor %d has numel < 0", i);
+    if (t.numel == 0) continue;
+    if (!t.grads) return fail(ZERO_EINVAL, "tensor %d: grads array is NULL", i);
+    for (int64_t k = 0; k < nbuf; ++k) {
+      if (!t.grads[k]) return fail(ZERO_EINVAL, "tensor %d: gradient pointer %lld is NULL", i,
+                                   (long long)k);
+      w->gptrs[(size_t)(i * nbuf + k)] = static_cast<const uint16_t*>(t.grads[k]);
+    }
+    if (need_state && ((!h->cfg.master16 && !t.master) || !t.m || !t.v || !t.param16))
+      return fail(ZERO_EINVAL, "tensor %d: master (unless master16), m, v and param16 must "
+                  "not be NULL", i);
+    Job jb;
+    jb.cfg = &h->cfg;
+    jb.g = w->gptrs.data() + (size_t)(i * nbuf);
+    jb.nbuf = (int)nbuf;
+    jb.n = t.numel;
+    jb.master = h->cfg.master16 ? nullptr : t.master;
+    jb.m = t.m;
+    jb.v = t.v;
+    jb.p16 = static_cast<uint16_t*>(t.param16);
+    w->jobs.push_back(jb);
+  }
+  w->number_blocks();
+  return ZERO_OK;
+}
+
+zero_opt_stats work_stats(zero_host_t h, const Work& w) {
   const int nt = h->pool->size();
   std::vector<Partial> part((size_t)nt);
   h->pool->run([&](int i) {
-    int64_t lo, hi;
-    range_of(jb, nt, i, &lo, &hi);
-    stats_range(jb, lo, hi, &part[(size_t)i]);
+    SqSum acc;
+    int bad = 0;
+    for_share(w, nt, i, [&](const Job& jb, int64_t lo, int64_t hi) {
+      stats_range(jb, lo, hi, &acc, &bad);
+    });
+    acc.into(part[(size_t)i].hi, part[(size_t)i].lo);
+    part[(size_t)i].nonfinite = bad;
   });
   double H = 0.0, L = 0.0;
   int bad = 0;
@@ -378,6 +454,30 @@ zero_opt_stats shard_stats(zero_host_t h, const Job& jb) {
   out.nonfinite = bad;
   out.reserved = 0;
   return out;
+}
+
+// Statistics (or the given global ones), the decision, and the update of
+// every run of `w`.
+zero_status step_work(zero_host_t h, int32_t rank, const Work& w, double divisor,
+                      double rk, const zero_opt_stats* global) {
+  const zero_opt_stats s = global ? *global : work_stats(h, w);
+  const zo::Hyper hp = zo::hyper_of(h->cfg, divisor > 0.0 ? divisor : rk);
+  zo::RankState& rs = h->ranks[(size_t)rank];
+  const zo::Decision d =
+      zo::decide_core(hp, rs, s.sumsq, s.nonfinite ? 1 : 0,
+                      [&hp](int64_t t, float* ss, float* isb2, float* decay) {
+                        zo::step_scalars(hp, t, ss, isb2, decay);
+                      });
+  h->last = d;
+  if (!d.skip && w.blocks() > 0) {
+    const int nt = h->pool->size();
+    h->pool->run([&](int i) {
+      for_share(w, nt, i, [&](const Job& jb, int64_t lo, int64_t hi) {
+        update_range(jb, d, lo, hi);
+      });
+    });
+  }
+  return ZERO_OK;
 }
 
 }  // namespace
@@ -432,47 +532,38 @@ zero_status zero_host_threads(zero_host_t h, int32_t* n_threads) {
 zero_status zero_host_grad_stats(zero_host_t h, int32_t rank, const zero_opt_buffers* bufs,
                                  zero_opt_stats* out) {
   if (!out) return fail(ZERO_EINVAL, "out is NULL");
-  std::vector<const uint16_t*> g;
-  Job jb;
-  zero_status st = make_job(h, rank, bufs, false, &g, &jb);
+  Work w;
+  zero_status st = flat_work(h, rank, bufs, false, &w);
   if (st != ZERO_OK) return st;
-  *out = shard_stats(h, jb);
+  *out = work_stats(h, w);
+  return ZERO_OK;
+}
+
+zero_status zero_host_grad_stats_tensors(zero_host_t h, int32_t rank,
+                                         const zero_opt_tensor_list* list, zero_opt_stats* out) {
+  if (!out) return fail(ZERO_EINVAL, "out is NULL");
+  Work w;
+  zero_status st = list_work(h, rank, list, false, &w);
+  if (st != ZERO_OK) return st;
+  *out = work_stats(h, w);
   return ZERO_OK;
 }
 
 zero_status zero_host_step(zero_host_t h, int32_t rank, const zero_opt_buffers* bufs,
                            const zero_opt_stats* global) {
-  std::vector<const uint16_t*> g;
-  Job jb;
-  zero_status st = make_job(h, rank, bufs, true, &g, &jb);
+  Work w;
+  zero_status st = flat_work(h, rank, bufs, true, &w);
   if (st != ZERO_OK) return st;
-  zero_opt_stats s;
-  if (global) {
-    s = *global;
-  } else {
-    s = shard_stats(h, jb);
-  }
-  const double divisor =
-      bufs->divisor > 0.0 ? bufs->divisor : (double)bufs->n_ranks * (double)bufs->n_micro;
-  const zo::Hyper hp = zo::hyper_of(h->cfg, divisor);
-  zo::RankState& rs = h->ranks[(size_t)rank];
-  const zo::Decision d =
-      zo::decide_core(hp, rs, s.sumsq, s.nonfinite ? 1 : 0,
-                      [&hp](int64_t t, float* ss, float* isb2, float* decay) {
-                        zo::step_scalars(hp, t, ss, isb2, decay);
-                      });
-  h->last = d;
-  if (!d.skip && jb.n > 0) {
-    const int nt = h->pool->size();
-    h->pool->run([&](int i) {
-      int64_t lo, hi;
-      range_of(jb, nt, i, &lo, &hi);
-      update_range(jb, d, lo, hi);
-    });
-  }
-  return ZERO_OK;
+  return step_work(h, rank, w, bufs->divisor, (double)bufs->n_ranks * bufs->n_micro, global);
 }
 
+zero_status zero_host_step_tensors(zero_host_t h, int32_t rank, const zero_opt_tensor_list* list,
+                                   const zero_opt_stats* global) {
+  Work w;
+  zero_status st = list_work(h, rank, list, true, &w);
+  if (st != ZERO_OK) return st;
+  return step_work(h, rank, w, list->divisor, (double)list->n_ranks * list->n_micro, global);
+}
 zero_status zero_host_loss_scale(zero_host_t h, int32_t rank, zero_opt_scaler_state* out) {
   zero_status st = check_rank(h, rank);
   if (st != ZERO_OK) return st;
