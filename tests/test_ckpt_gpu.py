@@ -95,3 +95,21 @@ def test_save_load_resume_is_bit_exact(tmp_path):
     assert torch.equal(a16.view(torch.int16), c16.view(torch.int16))
     z.zero_opt_destroy(h1)
     z.zero_opt_destroy(h3)
+
+
+def test_master16_handles_have_no_shard_files(tmp_path):
+    """A master16 handle keeps no fp32 masters, so shard files (which hold
+    them) are refused with ZERO_ENOTSUP before any work."""
+    import torch
+
+    import zero_sharded_mixed_05_gb300 as z
+    cfg = z.make_config(numel=1000, world=1, grad_dtype=z.BF16, master16=True)
+    h = z.zero_opt_create(cfg)
+    t = torch.zeros(1000, device="cuda:0")
+    with pytest.raises(z.ZeroOptError) as e:
+        z.zero_opt_save_shard(h, 0, None, t, t, str(tmp_path / "x.zshard"))
+    assert e.value.status == z.ZERO_ENOTSUP
+    with pytest.raises(z.ZeroOptError) as e:
+        z.zero_opt_load_shard(h, 0, None, t, t, str(tmp_path / "x.zshard"))
+    assert e.value.status == z.ZERO_ENOTSUP
+    z.zero_opt_destroy(h)
