@@ -251,6 +251,24 @@ zero_status zero_opt_grad_stats(zero_opt_t h, int32_t rank,
 zero_status zero_opt_fold_stats(const zero_opt_stats* per_rank, int32_t n,
                                 zero_opt_stats* out);
 
+/* The same two calls with the statistics kept on the device, so that a
+ * multi-process step needs no host round trip (the statistics go from rank to
+ * rank through a device collective, e.g. an all-gather of 16-byte records):
+ *
+ * zero_opt_grad_stats_async: as zero_opt_grad_stats, but the result is
+ * written into the DEVICE zero_opt_stats `out_dev` on `stream`; nothing
+ * synchronizes.
+ * zero_opt_step_folded: as zero_opt_step with the global statistics, where the
+ * fold of the n per-rank statistics at the DEVICE array `per_rank_dev` (rank
+ * order) is taken on the device, bit-identical to zero_opt_fold_stats.  The
+ * array is read when the step runs on `stream`.
+ * Errors: as zero_opt_grad_stats / zero_opt_step, plus EINVAL (out_dev or
+ * per_rank_dev NULL) and ERANGE (n outside [1, 2^20]). */
+zero_status zero_opt_grad_stats_async(zero_opt_t h, int32_t rank, const zero_opt_buffers* bufs,
+                                      void* stream, zero_opt_stats* out_dev);
+zero_status zero_opt_step_folded(zero_opt_t h, int32_t rank, const zero_opt_buffers* bufs,
+                                 void* stream, const zero_opt_stats* per_rank_dev, int32_t n);
+
 /* One optimizer step of `rank`'s shard (steps a1..a7), asynchronous on
  * `stream`.  `global` (host, may be NULL) is the fold of all ranks'
  * zero_opt_grad_stats for these same gradients; NULL means this shard is the

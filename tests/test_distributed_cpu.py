@@ -75,7 +75,8 @@ def _worker(rank, port, out_dir, code, master16):
     for step in range(1, STEPS + 1):
         grads = [torch.from_numpy(g.view(np.int16)).view(tdt)
                  for g in _local_grads(rank, step, scale, P, code)]
-        info = zs.step(grads, None if master16 else master, m, v, p16)
+        zs.step(grads, None if master16 else master, m, v, p16)
+        info = zs.last_step()
         infos.append((info.skipped, info.scale_used, info.t, info.coef))
         scale = z.zero_host_loss_scale(zs.h, rank).scale
     np.savez(os.path.join(out_dir, f"r{rank}.npz"), master=master.numpy(), m=m.numpy(),

@@ -64,7 +64,8 @@ def _worker(rank, port, out_path):
     for step in range(1, STEPS + 1):
         grads = [torch.from_numpy(g.view(np.int16)).view(torch.float16).to(dev)
                  for g in _grads(step, scale)]
-        info = zs.step(grads, master, m, v, p16)
+        zs.step(grads, master, m, v, p16)
+        info = zs.last_step()
         infos.append((info.skipped, info.scale_used, info.t))
         scale = z.zero_opt_loss_scale(zs.h, 0).scale
     torch.cuda.synchronize()

@@ -368,3 +368,57 @@ def test_low_precision_master_tensor_list(stash):
                    max_norm=0.5, sigma=1e-3, steps=3, ranks=2, micro=3, stash=stash,
                    master16=True)
     assert_flat_parity(res)
+
+
+def test_device_folded_statistics_equal_the_host_fold():
+    """zero_opt_grad_stats_async + zero_opt_step_folded (statistics kept and
+    folded on the device) against zero_opt_grad_stats + zero_opt_fold_stats +
+    zero_opt_step: three ranks of one buffer, four steps with an overflow on
+    the third, bit-identical states, decisions and scaler states."""
+    import torch
+
+    import zero_sharded_mixed_05_gb300 as z
+    dev = torch.device("cuda:0")
+    numel, world, R = 90_001, 3, 2
+    cfg = z.make_config(numel=numel, world=world, grad_dtype=z.BF16, lr=1e-3,
+                        weight_decay=0.01, max_grad_norm=0.3, dynamic_scale=True,
+                        init_scale=32.0)
+    hs = [z.zero_opt_create(cfg) for _ in range(2)]
+    _, _, S, P = z.zero_opt_shard_bounds(hs[0], 0)
+    p0 = torch.from_numpy(synth.normal_np(0x5EED0601, 0, 0, P, 0.02, synth.F32)).to(dev)
+    states = [[[p0[r * S:(r + 1) * S].clone(), torch.zeros(S, device=dev),
+                torch.zeros(S, device=dev)] for r in range(world)] for _ in range(2)]
+    p16 = [torch.zeros(P, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    stats = torch.zeros(16 * world, dtype=torch.uint8, device=dev)
+    for step in range(1, 5):
+        grads = [synth.normal_torch(0x5EED0601, 1 + b, P, 1e-2 * 32.0, synth.BF16, device=dev,
+                                    offset=step * P) for b in range(R)]
+        if step == 3:
+            grads[1][numel - 5] = float("inf")
+        # device fold
+        bufs = [z.make_buffers(*states[0][r], p16[0], grads) for r in range(world)]
+        for r in range(world):
+            z.zero_opt_grad_stats_async(hs[0], r, bufs[r], stats[16 * r:16 * (r + 1)])
+        for r in range(world):
+            z.zero_opt_step_folded(hs[0], r, bufs[r], stats, world)
+        dec = z.zero_opt_last_step(hs[0])
+        # host fold
+        bufs2 = [z.make_buffers(*states[1][r], p16[1], grads) for r in range(world)]
+        G = z.zero_opt_fold_stats([z.zero_opt_grad_stats(hs[1], r, bufs2[r])
+                                   for r in range(world)])
+        for r in range(world):
+            z.zero_opt_step(hs[1], r, bufs2[r], global_stats=G)
+        ref = z.zero_opt_last_step(hs[1])
+        assert (dec.skipped, dec.sumsq, dec.coef, dec.t) == (ref.skipped, ref.sumsq, ref.coef,
+                                                             ref.t) or (dec.skipped == ref.skipped == 1)
+        assert dec.skipped == (1 if step == 3 else 0)
+        for r in range(world):
+            assert z.zero_opt_loss_scale(hs[0], r).as_tuple() == \
+                z.zero_opt_loss_scale(hs[1], r).as_tuple()
+    torch.cuda.synchronize()
+    for r in range(world):
+        for a, b in zip(states[0][r], states[1][r]):
+            assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    assert torch.equal(p16[0].view(torch.int16), p16[1].view(torch.int16))
+    for h in hs:
+        z.zero_opt_destroy(h)

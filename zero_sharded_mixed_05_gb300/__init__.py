@@ -102,6 +102,8 @@ SIGNATURES = [
     ("zero_opt_grad_stats", _i32, [_vp, _i32, _P(zero_opt_buffers), _vp, _P(zero_opt_stats)]),
     ("zero_opt_fold_stats", _i32, [_P(zero_opt_stats), _i32, _P(zero_opt_stats)]),
     ("zero_opt_step", _i32, [_vp, _i32, _P(zero_opt_buffers), _vp, _P(zero_opt_stats)]),
+    ("zero_opt_grad_stats_async", _i32, [_vp, _i32, _P(zero_opt_buffers), _vp, _vp]),
+    ("zero_opt_step_folded", _i32, [_vp, _i32, _P(zero_opt_buffers), _vp, _vp, _i32]),
     ("zero_opt_grad_stats_tensors", _i32,
      [_vp, _i32, _P(zero_opt_tensor_list), _vp, _P(zero_opt_stats)]),
     ("zero_opt_step_tensors", _i32,
@@ -315,6 +317,22 @@ def zero_opt_step(h, rank: int, bufs: zero_opt_buffers, stream=None,
     gs = ctypes.byref(global_stats) if global_stats is not None else None
     _check(lib().zero_opt_step(h, rank, ctypes.byref(bufs), _stream(stream), gs),
            "zero_opt_step")
+
+
+def zero_opt_grad_stats_async(h, rank: int, bufs: zero_opt_buffers, out_dev,
+                              stream=None) -> None:
+    """Shard statistics into `out_dev`, a device buffer of 16 bytes (one
+    zero_opt_stats), without synchronizing."""
+    _check(lib().zero_opt_grad_stats_async(h, rank, ctypes.byref(bufs), _stream(stream),
+                                           _ptr(out_dev)), "zero_opt_grad_stats_async")
+
+
+def zero_opt_step_folded(h, rank: int, bufs: zero_opt_buffers, per_rank_dev, n: int,
+                         stream=None) -> None:
+    """Step with the global statistics folded on the device from `n` per-rank
+    zero_opt_stats records at `per_rank_dev` (device, rank order)."""
+    _check(lib().zero_opt_step_folded(h, rank, ctypes.byref(bufs), _stream(stream),
+                                      _ptr(per_rank_dev), n), "zero_opt_step_folded")
 
 
 def zero_opt_grad_stats_tensors(h, rank: int, lst: zero_opt_tensor_list,

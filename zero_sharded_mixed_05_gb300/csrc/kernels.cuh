@@ -488,14 +488,29 @@ static __device__ __noinline__ void decide(const Pass1Args& a, double own_sumsq,
   if (a.mode == kStatsOnly) {
     ws->own_sumsq = fault ? quiet_nan() : own_sumsq;
     ws->own_nonfinite = fault ? 1 : own_flag;
+    if (a.stats_out) {
+      a.stats_out->sumsq = ws->own_sumsq;
+      a.stats_out->nonfinite = ws->own_nonfinite;
+      a.stats_out->reserved = 0;
+    }
     return;
   }
   if (fault) {
     ws->dec = fault_decision(a.ranks[a.rank]);
     return;
   }
-  const double sumsq = a.mode == kStepGlobal ? a.g_sumsq : own_sumsq;
-  const int nonfinite = a.mode == kStepGlobal ? a.g_nonfinite : own_flag;
+  double sumsq = a.mode == kStepGlobal ? a.g_sumsq : own_sumsq;
+  int nonfinite = a.mode == kStepGlobal ? a.g_nonfinite : own_flag;
+  if (a.mode == kStepGlobalDev) {
+    // the scalar all-reduce, folded here in rank order exactly as
+    // zero_opt_fold_stats folds it on the host
+    sumsq = 0.0;
+    nonfinite = 0;
+    for (int r = 0; r < a.g_n; ++r) {
+      sumsq = __dadd_rn(sumsq, a.g_dev[r].sumsq);
+      if (a.g_dev[r].nonfinite) nonfinite = 1;
+    }
+  }
   RankState st = a.ranks[a.rank];
   // every stepping launch has a scalar CTA, which stored the scalars of step
   // t + 1 before this CTA could take the last ticket

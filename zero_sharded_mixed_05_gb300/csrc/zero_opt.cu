@@ -379,9 +379,13 @@ zero_status launch_kernel(zero_opt_t h, const void* fn, int grid, void* args,
 
 // Pass 1 (always: it takes the decision), then pass 2 unless only the
 // statistics are wanted.
+// `global`: host statistics (kStepGlobal) or, for kStepGlobalDev, `g_n`
+// per-rank device statistics; `stats_out`: device copy of a statistics-only
+// result, or NULL.
 zero_status run(zero_opt_t h, int32_t rank, const std::vector<HostRun>& runs, int nbuf,
                 double divisor, float* stash, void* stream_v, zo::Mode mode,
-                const zero_opt_stats* global) {
+                const zero_opt_stats* global, int32_t g_n = 0,
+                zero_opt_stats* stats_out = nullptr) {
   cudaStream_t stream = static_cast<cudaStream_t>(stream_v);
   float* use_stash = (stash != nullptr && nbuf > 4) ? stash : nullptr;
   Plan* plan = nullptr;
@@ -400,15 +404,21 @@ zero_status run(zero_opt_t h, int32_t rank, const std::vector<HostRun>& runs, in
   a1.nbuf = nbuf;
   // With the global statistics given and nothing to stash, pass 1 only
   // decides: one CTA, no tiles.
-  const bool reduce = !(mode == zo::kStepGlobal && use_stash == nullptr);
+  const bool reduce =
+      !((mode == zo::kStepGlobal || mode == zo::kStepGlobalDev) && use_stash == nullptr);
   a1.ntiles = reduce ? plan->ntiles : 0;
   a1.stash = use_stash;
   a1.mode = mode;
   a1.rank = rank;
-  if (global) {
+  if (global && mode == zo::kStepGlobal) {
     a1.g_sumsq = global->sumsq;
     a1.g_nonfinite = global->nonfinite ? 1 : 0;
   }
+  if (mode == zo::kStepGlobalDev) {
+    a1.g_dev = global;
+    a1.g_n = g_n;
+  }
+  a1.stats_out = stats_out;
   a1.hp = zo::hyper_of(h->cfg, divisor);
   a1.ws = h->ws;
   a1.ranks = h->ranks;
@@ -704,6 +714,39 @@ zero_status zero_opt_grad_stats(zero_opt_t h, int32_t rank, const zero_opt_buffe
   out->nonfinite = got.nonfinite;
   out->reserved = 0;
   return ZERO_OK;
+}
+
+zero_status zero_opt_grad_stats_async(zero_opt_t h, int32_t rank, const zero_opt_buffers* bufs,
+                                      void* stream, zero_opt_stats* out_dev) {
+  zero_status st = check_handle_rank(h, rank);
+  if (st != ZERO_OK) return st;
+  if (!out_dev) return fail(ZERO_EINVAL, "out_dev is NULL");
+  std::vector<HostRun> runs;
+  int nbuf = 0;
+  double divisor = 1.0;
+  st = flat_runs(h, rank, bufs, &runs, &nbuf, &divisor);
+  if (st != ZERO_OK) return st;
+  st = check_device(h);
+  if (st != ZERO_OK) return st;
+  return run(h, rank, runs, nbuf, divisor, bufs->stash, stream, zo::kStatsOnly, nullptr, 0,
+             out_dev);
+}
+
+zero_status zero_opt_step_folded(zero_opt_t h, int32_t rank, const zero_opt_buffers* bufs,
+                                 void* stream, const zero_opt_stats* per_rank_dev, int32_t n) {
+  zero_status st = check_handle_rank(h, rank);
+  if (st != ZERO_OK) return st;
+  if (!per_rank_dev) return fail(ZERO_EINVAL, "per_rank_dev is NULL");
+  if (n < 1 || n > (1 << 20)) return fail(ZERO_ERANGE, "n = %d outside [1, 2^20]", n);
+  std::vector<HostRun> runs;
+  int nbuf = 0;
+  double divisor = 1.0;
+  st = flat_runs(h, rank, bufs, &runs, &nbuf, &divisor);
+  if (st != ZERO_OK) return st;
+  st = check_device(h);
+  if (st != ZERO_OK) return st;
+  return run(h, rank, runs, nbuf, divisor, bufs->stash, stream, zo::kStepGlobalDev, per_rank_dev,
+             n);
 }
 
 zero_status zero_opt_fold_stats(const zero_opt_stats* per_rank, int32_t n,

@@ -87,7 +87,9 @@ struct Hyper {
   int64_t warmup_num_steps;
 };
 
-enum Mode : int32_t { kStepLocal = 0, kStepGlobal = 1, kStatsOnly = 2 };
+// kStepGlobalDev: the global statistics are folded on the device from the
+// per-rank statistics at g_dev (g_n of them, rank order).
+enum Mode : int32_t { kStepLocal = 0, kStepGlobal = 1, kStatsOnly = 2, kStepGlobalDev = 3 };
 
 struct Pass1Args {
   const Seg* segs;
@@ -107,6 +109,10 @@ struct Pass1Args {
   int32_t inject_wait_fault;   // test hook: leave one bulk-copy barrier un-armed
   int32_t scalar_cta;          // 1: the last CTA streams nothing and precomputes
                                // the next step's update scalars
+  const zero_opt_stats* g_dev; // kStepGlobalDev: per-rank statistics (device)
+  zero_opt_stats* stats_out;   // kStatsOnly: also written here (device), or NULL
+  int32_t g_n;
+  int32_t pad3;
 };
 
 struct Pass2Args {

@@ -19,8 +19,12 @@ How the exchanges are done here:
   order and precision of its own choosing; this way the result is bit-identical
   to the one-process step and to the oracle.  Each rank sends and receives
   (N-1)/N of its gradient bytes, the same volume as a ring reduce-scatter.
-- The scalar all-reduce is ``allgather_fold``: all statistics to all ranks,
-  folded in rank order, so every rank takes identical decisions.
+- The scalar all-reduce: every rank's 16-byte statistics record goes to every
+  rank, and each folds them in rank order, so every rank takes identical
+  decisions.  On the device back end this stays on the GPU
+  (zero_opt_grad_stats_async, an all-gather of the records,
+  zero_opt_step_folded), so a step never waits for the host; the host back
+  end uses ``allgather_fold``.
 - The all-gather of the updated 16-bit shards is ``all_gather_into_tensor``
   on their bytes.
 
@@ -32,8 +36,8 @@ from __future__ import annotations
 
 from . import (allgather_fold, make_buffers, zero_host_create, zero_host_destroy,
                zero_host_grad_stats, zero_host_last_step, zero_host_step, zero_opt_create,
-               zero_opt_destroy, zero_opt_grad_stats, zero_opt_last_step, zero_opt_shard_bounds,
-               zero_opt_step)
+               zero_opt_destroy, zero_opt_grad_stats_async, zero_opt_last_step,
+               zero_opt_shard_bounds, zero_opt_step_folded)
 
 
 def _bytes(t):
@@ -66,6 +70,7 @@ class Zero2Step:
         self.cfg = cfg
         self.S = -(-cfg.numel // cfg.world)
         self.P = self.S * cfg.world
+        self._stats = None   # device: every rank's statistics record (16 bytes each)
         if backend == "device":
             self.h = zero_opt_create(cfg)
             b, e, S, P = zero_opt_shard_bounds(self.h, self.rank)
@@ -109,21 +114,35 @@ class Zero2Step:
             dist.all_gather_into_tensor(out, _bytes(mine), group=self.group)
 
     def step(self, grads, master, m, v, param16, stream=None):
-        """Exchange, statistics, fold, step, all-gather; returns the step's
-        zero_opt_step_info (identical on every rank)."""
+        """Exchange, statistics, fold, step, all-gather.  On the device back
+        end every part is enqueued on the stream and nothing waits for the
+        host; last_step() reads the decision."""
         K = len(grads)
         mine = self.exchange_gradients(grads)
         bufs = make_buffers(master, m, v, param16, mine, n_ranks=self.world, n_micro=K,
                             grads_shard_local=True)
         if self.backend == "device":
-            own = zero_opt_grad_stats(self.h, self.rank, bufs, stream)
-            G = allgather_fold(own, self.group)
-            zero_opt_step(self.h, self.rank, bufs, stream, global_stats=G)
-            info = zero_opt_last_step(self.h, stream)
+            import torch
+            import torch.distributed as dist
+            if self._stats is None:
+                self._stats = torch.zeros(16 * self.world, dtype=torch.uint8,
+                                          device=mine[0].device)
+            own = self._stats[16 * self.rank:16 * (self.rank + 1)]
+            zero_opt_grad_stats_async(self.h, self.rank, bufs, own, stream)
+            if dist.get_backend(self.group) == "nccl":
+                dist.all_gather_into_tensor(self._stats, own, group=self.group)
+            else:
+                dist.all_gather_into_tensor(self._stats, own.clone(), group=self.group)
+            zero_opt_step_folded(self.h, self.rank, bufs, self._stats, self.world, stream)
         else:
             own = zero_host_grad_stats(self.h, self.rank, bufs)
             G = allgather_fold(own, self.group)
             zero_host_step(self.h, self.rank, bufs, global_stats=G)
-            info = zero_host_last_step(self.h)
         self.gather_params(param16)
-        return info
+
+    def last_step(self, stream=None):
+        """zero_opt_step_info of the last step (identical on every rank);
+        synchronizes the stream on the device back end."""
+        if self.backend == "device":
+            return zero_opt_last_step(self.h, stream)
+        return zero_host_last_step(self.h)
