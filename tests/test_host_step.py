@@ -269,3 +269,30 @@ def test_tensor_list(z, orc, threads, master16):
     assert skips == [0, 1, 0, 0]
     assert z.zero_host_loss_scale(h, 0).as_tuple() == sc.as_tuple()
     z.zero_host_destroy(h)
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_random_configuration(z, orc, seed):
+    """Seeded random layouts, buffers and optimizer settings: the host step
+    stays bit-identical to the oracle."""
+    rng = np.random.default_rng(1000 + seed)
+    gd = int(rng.choice([O.FP16, O.BF16]))
+    dynamic = bool(rng.integers(0, 2))
+    numel = int(rng.choice([1, 9, 4097, 30_001, 65_536]))
+    R, K = int(rng.integers(1, 4)), int(rng.integers(1, 3))
+    inject = {}
+    if dynamic and rng.integers(0, 2):
+        inject = {int(rng.integers(1, 4)): [(int(rng.integers(0, R * K)),
+                                             int(rng.integers(0, numel)),
+                                             0x7C00 if gd == O.FP16 else 0x7F80)]}
+    run_host(z, orc, numel=numel, world=int(rng.choice([1, 2, 3, 5])), R=R, K=K, gdtype=gd,
+             pdtype=int(rng.choice([O.FP16, O.BF16])), steps=3,
+             threads=int(rng.integers(1, 7)), lr=float(rng.choice([1e-4, 1e-3])),
+             wd=float(rng.choice([0.0, 0.05])), max_norm=float(rng.choice([0.0, 0.1, 1.0])),
+             dynamic=dynamic, init_scale=float(rng.choice([1.0, 256.0])) if dynamic else 1.0,
+             window=int(rng.choice([2, 1000])), hysteresis=int(rng.choice([1, 2])),
+             warmup=(0.0, 0.0, 0) if rng.integers(0, 2) else (1e-5, 1e-3, 2),
+             sigma=float(rng.choice([1e-3, 1e-2])), seed=0x5EED0B00 + seed,
+             inject=inject, grads_local=bool(rng.integers(0, 2)),
+             p16_local=bool(rng.integers(0, 2)), master16=bool(rng.integers(0, 3) == 0),
+             bias_correction=bool(rng.integers(0, 4) != 0))
