@@ -39,16 +39,13 @@ ZO_HD inline double quiet_nan() {
 }
 
 // Update scalars of Adam step t, computed in binary64 and rounded once to
-// binary32: step_size = lr / (1 - beta1^t), isb2 = 1 / sqrt(1 - beta2^t) (both
-// corrections 1 without bias correction) and the decoupled decay 1 - lr * wd,
-// where lr is WarmupLR's value when warmup_num_steps > 0.
-ZO_HD inline void step_scalars(const Hyper& hp, int64_t t, float* step_size, float* isb2,
-                               float* decay) {
-  double bc1 = 1.0, bc2 = 1.0;
-  if (hp.bias_correction) {
-    bc1 = 1.0 - pow(hp.beta1, (double)t);
-    bc2 = 1.0 - pow(hp.beta2, (double)t);
-  }
+// binary32: step_size = lr / bc1, isb2 = 1 / sqrt(bc2) with the bias
+// corrections bc1 = 1 - beta1^t, bc2 = 1 - beta2^t (both 1 without bias
+// correction), and the decoupled decay 1 - lr * wd, where lr is WarmupLR's
+// value when warmup_num_steps > 0.
+ZO_HD inline void step_scalars_bc(const Hyper& hp, int64_t t, double bc1, double bc2,
+                                  float* step_size, float* isb2, float* decay) {
+  if (!hp.bias_correction) bc1 = bc2 = 1.0;
   double lr = hp.lr;
   if (hp.warmup_num_steps > 0) {
     const double T = (double)hp.warmup_num_steps;
@@ -60,13 +57,22 @@ ZO_HD inline void step_scalars(const Hyper& hp, int64_t t, float* step_size, flo
   *decay = (float)(1.0 - lr * hp.wd);
 }
 
+// The bias corrections of Adam step t: 1 - beta1^t and 1 - beta2^t.
+ZO_HD inline double bias_correction(double beta, int64_t t) { return 1.0 - pow(beta, (double)t); }
+
+ZO_HD inline void step_scalars(const Hyper& hp, int64_t t, float* step_size, float* isb2,
+                               float* decay) {
+  step_scalars_bc(hp, t, bias_correction(hp.beta1, t), bias_correction(hp.beta2, t), step_size,
+                  isb2, decay);
+}
+
 // The decision of one step of a rank whose scaler state is `st` (updated in
 // place), from the global statistics.  `scalars(t, &step_size, &isb2,
 // &decay)` supplies the update scalars of Adam step t: step_scalars itself,
 // or values computed ahead of time.
 template <typename Scalars>
 ZO_HD inline Decision decide_core(const Hyper& hp, RankState& st, double sumsq, int nonfinite,
-                                  Scalars scalars) {
+                                  Scalars scalars, const double* inv_pre = nullptr) {
   Decision d;
   d.fault = 0;
   d.pad_ = 0;
@@ -76,7 +82,8 @@ ZO_HD inline Decision decide_core(const Hyper& hp, RankState& st, double sumsq, 
   d.coef = 0.0f;
   d.step_size = d.isb2 = d.decay = d.b1 = d.omb1 = d.b2 = d.omb2 = d.eps = 0.0f;
   const float scale = st.scale;
-  const double inv = 1.0 / ((double)scale * hp.divisor);
+  // inv_pre: the same quotient, computed ahead for this scale
+  const double inv = inv_pre ? *inv_pre : 1.0 / ((double)scale * hp.divisor);
   if (nonfinite) {
     d.skip = 1;
     d.norm = quiet_nan();

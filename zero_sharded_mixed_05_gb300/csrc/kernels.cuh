@@ -465,10 +465,30 @@ __device__ __forceinline__ double block_sum(double x, double* red) {
 // decision, which waits for every CTA, does no binary64 pow.
 static __device__ __noinline__ void precompute_scalars(const Pass1Args& a) {
   PreScalars p;
-  p.t = a.ranks[a.rank].t + 1;
-  step_scalars(a.hp, p.t, &p.step_size, &p.isb2, &p.decay);
+  const RankState st = a.ranks[a.rank];
+  p.t = st.t + 1;
+  if (a.bc_table && p.t <= kBcSteps) {
+    const double* bc = a.bc_table + 2 * (p.t - 1);
+    step_scalars_bc(a.hp, p.t, bc[0], bc[1], &p.step_size, &p.isb2, &p.decay);
+  } else {
+    step_scalars(a.hp, p.t, &p.step_size, &p.isb2, &p.decay);
+  }
   p.pad_ = 0;
+  p.inv = 1.0 / ((double)st.scale * a.hp.divisor);
   a.ws->pre = p;
+}
+
+// Bias-correction table of a handle: entry t - 1 holds 1 - beta1^t and
+// 1 - beta2^t, exactly as the decision computes them.
+struct BcTableArgs {
+  double* table;
+  double beta1, beta2;
+};
+static __global__ void __launch_bounds__(kThreads) bc_table_kernel(const BcTableArgs a) {
+  const int64_t i = blockIdx.x * (int64_t)kThreads + threadIdx.x;
+  if (i >= kBcSteps) return;
+  a.table[2 * i] = bias_correction(a.beta1, i + 1);
+  a.table[2 * i + 1] = bias_correction(a.beta2, i + 1);
 }
 
 // True for the CTA that streams nothing (the last one, when scalar_cta is set).
@@ -515,12 +535,14 @@ static __device__ __noinline__ void decide(const Pass1Args& a, double own_sumsq,
   // every stepping launch has a scalar CTA, which stored the scalars of step
   // t + 1 before this CTA could take the last ticket
   const volatile PreScalars* pre = &ws->pre;
+  const double inv = pre->inv;
   const Decision d = decide_core(a.hp, st, sumsq, nonfinite,
                                  [pre](int64_t, float* ss, float* isb2, float* decay) {
                                    *ss = pre->step_size;
                                    *isb2 = pre->isb2;
                                    *decay = pre->decay;
-                                 });
+                                 },
+                                 &inv);
   a.ranks[a.rank] = st;
   ws->dec = d;
 }

@@ -148,6 +148,7 @@ struct zero_opt_handle {
   int sms = 0;
   zo::Workspace* ws = nullptr;
   zo::RankState* ranks = nullptr;
+  double* bc_table = nullptr;  // device bias corrections of steps 1..kBcSteps
   void* pinned = nullptr;  // page-locked staging for small reads
   int64_t launches = 0;
   uint64_t clock = 0;
@@ -422,6 +423,7 @@ zero_status run(zero_opt_t h, int32_t rank, const std::vector<HostRun>& runs, in
   a1.hp = zo::hyper_of(h->cfg, divisor);
   a1.ws = h->ws;
   a1.ranks = h->ranks;
+  a1.bc_table = h->bc_table;
   a1.inject_wait_fault = h->inject_wait_fault;
   h->inject_wait_fault = 0;
 
@@ -432,8 +434,14 @@ zero_status run(zero_opt_t h, int32_t rank, const std::vector<HostRun>& runs, in
   // end of the launch does none; it takes one of the resident slots so that
   // every CTA runs at once.
   a1.scalar_cta = mode != zo::kStatsOnly ? 1 : 0;
+  // work units: tiles, or the bulk kernel's chunks of 4 or 8 tiles
+  int64_t units = a1.ntiles;
+  if (ZO_PASS1_BULK && nbuf == 1 && use_stash == nullptr) {
+    const int64_t ct = plan->ntiles >= kBigChunkTiles ? 8 : 4;
+    units = (a1.ntiles + ct - 1) / ct;
+  }
   int64_t g1 = (int64_t)occupancy(h, f1) * h->sms - a1.scalar_cta;
-  g1 = std::min<int64_t>(g1, std::max<int64_t>(a1.ntiles, 1));
+  g1 = std::min<int64_t>(g1, std::max<int64_t>(units, 1));
   g1 = std::max<int64_t>(std::min<int64_t>(g1, zo::kMaxCtas - 1), 1) + a1.scalar_cta;
   if (h->ev[0]) cudaEventRecord(h->ev[0], stream);
   st = launch_kernel(h, f1, (int)g1, &a1, stream);
@@ -632,7 +640,22 @@ zero_status zero_opt_create(const zero_opt_config* cfg, zero_opt_t* out) {
   }
   e = cudaMemcpy(ws, init.data(), ws_bytes, cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMallocHost(&h->pinned, kPinnedBytes);
+  if (e == cudaSuccess) e = cudaMalloc(&h->bc_table, sizeof(double) * 2 * zo::kBcSteps);
+  if (e == cudaSuccess) {
+    zo::BcTableArgs ta;
+    ta.table = h->bc_table;
+    ta.beta1 = cfg->beta1;
+    ta.beta2 = cfg->beta2;
+    void* params[] = {&ta};
+    e = cudaLaunchKernel(reinterpret_cast<const void*>(zo::bc_table_kernel),
+                         dim3((unsigned)((zo::kBcSteps + zo::kThreads - 1) / zo::kThreads)),
+                         dim3(zo::kThreads), params, 0, nullptr);
+    // ready before any stream, blocking or not, can use the handle
+    if (e == cudaSuccess) e = cudaStreamSynchronize(nullptr);
+  }
   if (e != cudaSuccess) {
+    cudaFree(h->bc_table);
+    if (h->pinned) cudaFreeHost(h->pinned);
     cudaFree(ws);
     delete h;
     return cuda_fail(e, "zero_opt_create");
@@ -654,6 +677,7 @@ zero_status zero_opt_destroy(zero_opt_t h) {
       delete p;
     }
     cudaFree(h->ws);
+    cudaFree(h->bc_table);
     cudaFreeHost(h->pinned);
     if (prev >= 0) cudaSetDevice(prev);
   }

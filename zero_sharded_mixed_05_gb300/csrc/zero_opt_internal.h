@@ -64,7 +64,12 @@ struct PreScalars {
   int64_t t;             // the step they belong to; 0: none
   float step_size, isb2, decay;
   int32_t pad_;
+  double inv;            // 1 / (scale * divisor) for the scale of this launch
 };
+
+// Steps whose bias corrections are tabulated per handle (computed on the
+// device at creation with the same pow as the decision's fallback).
+constexpr int64_t kBcSteps = 1 << 16;
 
 struct Workspace {
   unsigned int ticket;   // CTAs of pass 1 that finished; reset by the last
@@ -109,6 +114,7 @@ struct Pass1Args {
   int32_t inject_wait_fault;   // test hook: leave one bulk-copy barrier un-armed
   int32_t scalar_cta;          // 1: the last CTA streams nothing and precomputes
                                // the next step's update scalars
+  const double* bc_table;      // [kBcSteps][2]: 1 - beta1^t, 1 - beta2^t for t = 1..kBcSteps
   const zero_opt_stats* g_dev; // kStepGlobalDev: per-rank statistics (device)
   zero_opt_stats* stats_out;   // kStatsOnly: also written here (device), or NULL
   int32_t g_n;
