@@ -37,7 +37,9 @@
  *     for every call on the handle.  "host" pointers are ordinary CPU memory.
  *   - The library never allocates, frees or retains caller buffers.  Device
  *     buffers must stay valid until the stream has passed the work that uses
- *     them.  The handle owns a small device workspace (a few tens of KB).
+ *     them.  The handle owns a small device workspace (about 1.1 MB: the
+ *     pass-1 partials and decision, the scaler replicas and a table of the
+ *     Adam bias corrections of the first 65536 steps).
  *   - `stream` is a cudaStream_t (NULL is the legacy default stream).  Work is
  *     enqueued asynchronously unless the function says it synchronizes.
  *   - Calls on one handle must be ordered (one stream, or externally
