@@ -71,6 +71,7 @@ class Zero2Step:
         self.S = -(-cfg.numel // cfg.world)
         self.P = self.S * cfg.world
         self._stats = None   # device: every rank's statistics record (16 bytes each)
+        self._recv = None    # all-to-all receive buffers, one per micro-step
         if backend == "device":
             self.h = zero_opt_create(cfg)
             b, e, S, P = zero_opt_shard_bounds(self.h, self.rank)
@@ -89,15 +90,16 @@ class Zero2Step:
         import torch
         import torch.distributed as dist
         S, N = self.S, self.world
-        recv = []
-        for g in grads:
+        K = len(grads)
+        # receive buffers are kept from step to step (no allocation per step)
+        if (self._recv is None or len(self._recv) != K or self._recv[0].dtype != grads[0].dtype
+                or self._recv[0].device != grads[0].device):
+            self._recv = [torch.empty_like(g) for g in grads]
+        for g, out in zip(grads, self._recv):
             if g.numel() != self.P:
                 raise ValueError(f"gradient buffers must hold P = {self.P} elements")
-            out = torch.empty_like(g)
             dist.all_to_all_single(_bytes(out), _bytes(g), group=self.group)
-            recv.append(out)
-        K = len(grads)
-        return [recv[k][j * S:(j + 1) * S] for j in range(N) for k in range(K)]
+        return [self._recv[k][j * S:(j + 1) * S] for j in range(N) for k in range(K)]
 
     def gather_params(self, param16):
         """All-gather of the 16-bit shards into the full padded buffer."""
