@@ -33,3 +33,19 @@ def read_golden(name):
             if line:
                 rows.append(line.split())
     return rows
+
+
+def spawn_bounded(fn, args, nprocs, seconds=300):
+    """torch.multiprocessing.spawn with a time limit: children still running
+    after `seconds` are terminated and the test fails instead of waiting."""
+    import time
+
+    import torch.multiprocessing as tmp
+    ctx = tmp.spawn(fn, args=args, nprocs=nprocs, join=False)
+    deadline = time.time() + seconds
+    while not ctx.join(timeout=5):
+        if time.time() > deadline:
+            for p in ctx.processes:
+                if p.is_alive():
+                    p.terminate()
+            raise AssertionError(f"spawned ranks did not finish within {seconds} s")

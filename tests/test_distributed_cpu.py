@@ -10,7 +10,8 @@ import socket
 
 import numpy as np
 import pytest
-import torch.multiprocessing as mp
+
+from conftest import spawn_bounded
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 NUMEL = 100_003          # odd: the last shard has padding
@@ -93,8 +94,7 @@ def test_two_rank_zero2_step_matches_the_oracle(tmp_path, code, master16):
     _build.build()
     import oracle as O
     import synth
-    mp.spawn(_worker, args=(_free_port(), str(tmp_path), code, master16), nprocs=WORLD,
-             join=True)
+    spawn_bounded(_worker, (_free_port(), str(tmp_path), code, master16), WORLD)
     res = [np.load(os.path.join(tmp_path, f"r{r}.npz")) for r in range(WORLD)]
     # the oracle: the one-process step of every shard with R = WORLD ranks' K buffers each
     orc = O.default()

@@ -11,7 +11,8 @@ import socket
 
 import numpy as np
 import pytest
-import torch.multiprocessing as mp
+
+from conftest import spawn_bounded
 
 pytestmark = pytest.mark.gpu
 
@@ -84,7 +85,7 @@ def test_one_rank_device_zero2_step(tmp_path):
     import oracle as O
     import synth
     out = os.path.join(tmp_path, "r0.npz")
-    mp.spawn(_worker, args=(_free_port(), out), nprocs=1, join=True)
+    spawn_bounded(_worker, (_free_port(), out), 1)
     got = np.load(out)
     orc = O.default()
     hp = O.hparams(lr=1e-3, weight_decay=0.01, dynamic_scale=True, scale_window=1000)

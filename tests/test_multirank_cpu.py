@@ -7,7 +7,8 @@ import socket
 
 import numpy as np
 import pytest
-import torch.multiprocessing as mp
+
+from conftest import spawn_bounded
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 NUMEL = 100_003
@@ -60,8 +61,7 @@ def test_two_rank_stats_exchange(tmp_path, inject):
     _build.build()
     import oracle as O
     world = 2
-    mp.spawn(_worker, args=(world, _free_port(), str(tmp_path), inject), nprocs=world,
-             join=True)
+    spawn_bounded(_worker, (world, _free_port(), str(tmp_path), inject), world)
     rows = [np.load(os.path.join(tmp_path, f"r{r}.npy")) for r in range(world)]
     assert rows[0][0].tobytes() == rows[1][0].tobytes()        # identical bits
     assert rows[0][1] == rows[1][1] == float(inject)
