@@ -12,7 +12,7 @@ import pytest
 import oracle as O
 import synth
 from harness import (FlatCase, assert_flat_parity, exact_fraction, llama_like_shapes,
-                     run_flat, run_list, ulp16_diff)
+                     run_flat, run_list, to_np16, ulp16_diff)
 
 pytestmark = pytest.mark.gpu
 
@@ -422,3 +422,42 @@ def test_device_folded_statistics_equal_the_host_fold():
     assert torch.equal(p16[0].view(torch.int16), p16[1].view(torch.int16))
     for h in hs:
         z.zero_opt_destroy(h)
+
+
+@pytest.mark.parametrize("t0,warmup", [(65_533, (0.0, 0.0, 0)), (65_534, (1e-5, 1e-3, 70_000))])
+def test_steps_across_the_bias_correction_table(t0, warmup):
+    """The bias corrections of steps 1..65536 come from a per-handle table, later
+    ones from pow on the device: steps t0+1 .. t0+4 straddle the boundary
+    (with WarmupLR still ramping in the second case) and must match the
+    oracle bit for bit, as the scaler counters must."""
+    import torch
+
+    import zero_sharded_mixed_05_gb300 as z
+    dev = torch.device("cuda:0")
+    n = 50_003
+    cfg = z.make_config(numel=n, world=1, grad_dtype=z.BF16, lr=1e-3, weight_decay=0.01,
+                        dynamic_scale=False, init_scale=1.0, warmup=warmup)
+    h = z.zero_opt_create(cfg)
+    st = z.zero_opt_loss_scale(h, 0)
+    st.t = t0
+    z.zero_opt_set_loss_scale(h, 0, st)
+    hp = O.hparams(lr=1e-3, weight_decay=0.01, warmup=warmup)
+    sc = O.scaler(1.0)
+    sc.t = t0
+    orc = O.default()
+    p0 = synth.normal_np(0x5EED0701, 0, 0, n, 0.02, synth.F32)
+    state = [torch.from_numpy(p0).to(dev), torch.zeros(n, device=dev), torch.zeros(n, device=dev),
+             torch.zeros(n, dtype=torch.bfloat16, device=dev)]
+    ref = [p0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32), np.zeros(n, np.uint16)]
+    for step in range(1, 5):
+        g = synth.normal_np(0x5EED0701, 1, step * n, n, 1e-2, synth.BF16)
+        gt = torch.from_numpy(g.view(np.int16)).view(torch.bfloat16).to(dev)
+        z.zero_opt_step(h, 0, z.make_buffers(*state, [gt]))
+        orc.step(hp, sc, [g], O.BF16, *ref, O.BF16, 1.0)
+        assert z.zero_opt_loss_scale(h, 0).as_tuple() == sc.as_tuple()
+    torch.cuda.synchronize()
+    assert sc.t == t0 + 4
+    for a, b in zip(state[:3], ref[:3]):
+        assert (a.cpu().numpy().view(np.uint32) == b.view(np.uint32)).all()
+    assert (to_np16(state[3]) == ref[3]).all()
+    z.zero_opt_destroy(h)
