@@ -331,6 +331,17 @@ struct SqAcc {
     L = f2_add(L, f2_add(f2_sub(H, AP), f2_sub(P, BP)));
     H = T;
   }
+  // The same accumulation when every lane of H is at least the square being
+  // added: Dekker's Fast2Sum, whose error term (H + P) - T is exact under
+  // that condition and therefore bit-identical to TwoSum's, in four packed
+  // operations instead of seven.
+  static __device__ __forceinline__ void pair_fast_into(f32x2& H, f32x2& L, float a, float b) {
+    const f32x2 X = f2_pack(a, b);
+    const f32x2 P = f2_mul(X, X);
+    const f32x2 T = f2_add(H, P);
+    L = f2_add(L, f2_sub(P, f2_sub(T, H)));
+    H = T;
+  }
 #endif
   __device__ __forceinline__ void pair_exact(float a, float b) {
 #if ZO_PACKED_SQ
@@ -406,12 +417,27 @@ struct SqAcc {
     if (Fmt<GT>::fast16(t16)) {
       const uint32_t w[4] = {r.x, r.y, r.z, r.w};
       const uint32_t u[4] = {q.x, q.y, q.z, q.w};
+      // The sums only grow (the squares are >= 0), so if the smallest of the
+      // four running sums is at least the largest square of the sixteen, each
+      // addition meets Fast2Sum's condition |H| >= |P|.
+      const float mx = Fmt<GT>::dec((unsigned short)t16);
+      const float hmin = fminf(fminf(f2_lo(H), f2_hi(H)), fminf(f2_lo(H2), f2_hi(H2)));
+      if (hmin >= __fmul_rn(mx, mx)) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 x = Fmt<GT>::dec2(w[k]);
-        const float2 y = Fmt<GT>::dec2(u[k]);
-        pair_exact_into(H, L, x.x, x.y);
-        pair_exact_into(H2, L2, y.x, y.y);
+        for (int k = 0; k < 4; ++k) {
+          const float2 x = Fmt<GT>::dec2(w[k]);
+          const float2 y = Fmt<GT>::dec2(u[k]);
+          pair_fast_into(H, L, x.x, x.y);
+          pair_fast_into(H2, L2, y.x, y.y);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 x = Fmt<GT>::dec2(w[k]);
+          const float2 y = Fmt<GT>::dec2(u[k]);
+          pair_exact_into(H, L, x.x, x.y);
+          pair_exact_into(H2, L2, y.x, y.y);
+        }
       }
     } else {
       add_raw16<GT>(r);
