@@ -13,7 +13,9 @@
 //   waiting) folds the partials in CTA order in binary64, takes the per-step
 //   decisions (skip, clip coefficient, Adam scalars) and advances the rank's
 //   loss-scaler state.  One extra CTA computes the next step's binary64
-//   scalars while the others stream.
+//   scalars while the others stream.  Pass 1 is a programmatic dependent
+//   launch of whatever precedes it on the stream and waits for it at its
+//   very start.
 // pass2_kernel (steps a5..a7): a programmatic dependent launch of pass 1; it
 //   reads the decision, and on a skip every CTA returns at once; otherwise it
 //   applies unscale x clip, AdamW on the fp32 master copy (or the widened
@@ -214,6 +216,19 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 __device__ __forceinline__ void pdl_wait() {
 #if ZO_PDL
   asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+}
+// Pass 1 as a dependent launch of whatever kernel precedes it on the stream
+// (the previous step's pass 2, or the caller's last kernel): its CTAs may be
+// scheduled before that kernel ends, and wait at their very start, before
+// any memory access, for it to complete with all its memory visible.
+#ifndef ZO_PDL_PASS1
+#define ZO_PDL_PASS1 1
+#endif
+__device__ __forceinline__ void pass1_prologue() {
+  pdl_launch_dependents();
+#if ZO_PDL_PASS1
+  pdl_wait();
 #endif
 }
 // Warm L2 with `bytes` at `p` (16-byte aligned, a multiple of 16 bytes).
@@ -464,6 +479,9 @@ struct SqAcc {
   }
 };
 
+#ifndef ZO_BLOCKSUM_TREE
+#define ZO_BLOCKSUM_TREE 0
+#endif
 // Fixed-shape CTA sum in binary64: the result (valid in thread 0) depends only
 // on the inputs, never on timing.
 __device__ __forceinline__ double block_sum(double x, double* red) {
@@ -473,10 +491,19 @@ __device__ __forceinline__ double block_sum(double x, double* red) {
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = x;
   __syncthreads();
   double t = 0.0;
+#if ZO_BLOCKSUM_TREE
+  if (threadIdx.x < 32) {
+    t = threadIdx.x < kThreads / 32 ? red[threadIdx.x] : 0.0;
+#pragma unroll
+    for (int off = kThreads / 64; off > 0; off >>= 1)
+      t = __dadd_rn(t, __shfl_down_sync(0xffffffffu, t, off));
+  }
+#else
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int w = 0; w < kThreads / 32; ++w) t = __dadd_rn(t, red[w]);
   }
+#endif
   return t;
 }
 
@@ -526,10 +553,39 @@ __device__ __forceinline__ bool is_scalar_cta(const Pass1Args& a) {
 // publishes its statistics (after a fault: an overflow, so that every rank
 // that folds them skips).  A fault skips the step and leaves the scaler state
 // alone.  Otherwise the rank's scaler replica advances through decide_core.
-static __device__ __noinline__ void decide(const Pass1Args& a, double own_sumsq, int own_flag) {
+// The decision's inputs from memory: the fault flag, the rank's scaler state
+// and the scalar CTA's precomputed scalars.  The last CTA's thread 0 loads
+// them (from L2: they were written by other CTAs of this launch or by the
+// previous one) before it folds the partials, so that their latency overlaps
+// the fold instead of following it.
+struct DecideInputs {
+  RankState st;
+  PreScalars pre;
+  int32_t fault;
+};
+template <typename T>
+__device__ __forceinline__ T ldcg_struct(const T* p) {
+  static_assert(sizeof(T) % 8 == 0 && alignof(T) >= 8, "8-byte words");
+  T v;
+  const long long* src = reinterpret_cast<const long long*>(p);
+  long long* dst = reinterpret_cast<long long*>(&v);
+#pragma unroll
+  for (int i = 0; i < (int)(sizeof(T) / 8); ++i) dst[i] = __ldcg(src + i);
+  return v;
+}
+__device__ __forceinline__ DecideInputs load_decide_inputs(const Pass1Args& a) {
+  DecideInputs in;
+  in.fault = __ldcg(&a.ws->fault);
+  in.st = ldcg_struct(a.ranks + a.rank);
+  in.pre = ldcg_struct(&a.ws->pre);
+  return in;
+}
+
+static __device__ __forceinline__ void decide(const Pass1Args& a, double own_sumsq, int own_flag,
+                                           const DecideInputs in) {
   Workspace* ws = a.ws;
   ws->ticket = 0u;
-  const int fault = ws->fault;
+  const int fault = in.fault;
   ws->fault = 0;
   if (a.mode == kStatsOnly) {
     ws->own_sumsq = fault ? quiet_nan() : own_sumsq;
@@ -542,7 +598,7 @@ static __device__ __noinline__ void decide(const Pass1Args& a, double own_sumsq,
     return;
   }
   if (fault) {
-    ws->dec = fault_decision(a.ranks[a.rank]);
+    ws->dec = fault_decision(in.st);
     return;
   }
   double sumsq = a.mode == kStepGlobal ? a.g_sumsq : own_sumsq;
@@ -557,16 +613,16 @@ static __device__ __noinline__ void decide(const Pass1Args& a, double own_sumsq,
       if (a.g_dev[r].nonfinite) nonfinite = 1;
     }
   }
-  RankState st = a.ranks[a.rank];
+  RankState st = in.st;
   // every stepping launch has a scalar CTA, which stored the scalars of step
   // t + 1 before this CTA could take the last ticket
-  const volatile PreScalars* pre = &ws->pre;
-  const double inv = pre->inv;
+  const PreScalars& pre = in.pre;
+  const double inv = pre.inv;
   const Decision d = decide_core(a.hp, st, sumsq, nonfinite,
-                                 [pre](int64_t, float* ss, float* isb2, float* decay) {
-                                   *ss = pre->step_size;
-                                   *isb2 = pre->isb2;
-                                   *decay = pre->decay;
+                                 [&pre](int64_t, float* ss, float* isb2, float* decay) {
+                                   *ss = pre.step_size;
+                                   *isb2 = pre.isb2;
+                                   *decay = pre.decay;
                                  },
                                  &inv);
   a.ranks[a.rank] = st;
@@ -574,6 +630,22 @@ static __device__ __noinline__ void decide(const Pass1Args& a, double own_sumsq,
 }
 
 // ------------------------------------------------------------- pass 1
+// The ticket of the last-CTA fold.  Every write another CTA needs (its
+// partial and flag, the scalar CTA's precomputed scalars, a fault flag) is
+// made by the CTA's thread 0 before it takes the ticket, and the atomic
+// increment has release and acquire semantics at GPU scope: the CTA that
+// draws the last ticket synchronizes with every earlier increment (they form
+// one release sequence), and its barrier then orders its other threads'
+// loads after all of those writes.
+#ifndef ZO_TICKET_ACQREL
+#define ZO_TICKET_ACQREL 1
+#endif
+__device__ __forceinline__ unsigned int ticket_add_acq_rel(unsigned int* p) {
+  unsigned int old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
+  return old;
+}
+
 // The epilogue shared by both pass-1 kernels: one binary64 partial and one
 // overflow flag per CTA; the CTA that finishes last folds them in CTA order
 // and takes the decisions.
@@ -585,22 +657,44 @@ __device__ __forceinline__ void pass1_finish(const Pass1Args& a, double mine, in
   if (tid == 0) {
     a.ws->part_sumsq[blockIdx.x] = blk;
     a.ws->part_flag[blockIdx.x] = any;
+#if ZO_TICKET_ACQREL
+    const unsigned int prev = ticket_add_acq_rel(&a.ws->ticket);
+#else
     __threadfence();
     const unsigned int prev = atomicAdd(&a.ws->ticket, 1u);
+#endif
     *s_last = (prev == gridDim.x - 1) ? 1 : 0;
   }
   __syncthreads();
   if (!*s_last) return;
+#if !ZO_TICKET_ACQREL
   __threadfence();
+#endif
+  DecideInputs in;
+  if (tid == 0) in = load_decide_inputs(a);
+  // each thread folds the partials c = tid, tid + 256, ... in that order; the
+  // loads of four are issued before any is added (past the grid: +0, which
+  // leaves the sum unchanged)
   double part = 0.0;
   int f = 0;
-  for (int c = tid; c < (int)gridDim.x; c += kThreads) {
-    part = __dadd_rn(part, __ldcg(&a.ws->part_sumsq[c]));
-    f |= __ldcg(&a.ws->part_flag[c]);
+  for (int c0 = 0; c0 < (int)gridDim.x; c0 += 4 * kThreads) {
+    double v[4];
+    int fl[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int c = c0 + k * kThreads + tid;
+      v[k] = c < (int)gridDim.x ? __ldcg(&a.ws->part_sumsq[c]) : 0.0;
+      fl[k] = c < (int)gridDim.x ? __ldcg(&a.ws->part_flag[c]) : 0;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      part = __dadd_rn(part, v[k]);
+      f |= fl[k];
+    }
   }
   const double tot = block_sum(part, red);
   const int anyf = __syncthreads_or(f);
-  if (tid == 0) decide(a, tot, anyf);
+  if (tid == 0) decide(a, tot, anyf, in);
 }
 
 // One tile element by element: a ragged tail of a vector run (e >= e0 within
@@ -642,7 +736,7 @@ __device__ __noinline__ Sums8 pass1_elementwise_sums(const Pass1Args& a, int64_t
 template <typename GT>
 __global__ void __launch_bounds__(kThreads, ZO_PASS1_MIN_CTAS)
     pass1_single_kernel(const Pass1Args a) {
-  pdl_launch_dependents();
+  pass1_prologue();
   __shared__ double red[kThreads / 32];
   __shared__ int s_last;
   constexpr int U = ZO_PASS1_UNROLL;
@@ -770,7 +864,7 @@ constexpr int bulk_min_ctas(int chunk_tiles) { return chunk_tiles >= 8 ? 3 : ZO_
 template <typename GT, int CT>
 __global__ void __launch_bounds__(kThreads, bulk_min_ctas(CT))
     pass1_bulk_kernel(const Pass1Args a) {
-  pdl_launch_dependents();
+  pass1_prologue();
   constexpr int S = ZO_BULK_STAGES;
   constexpr int kChunkTiles = CT;
   extern __shared__ __align__(128) uint4 stage_buf[];  // [S][CT][kThreads]
@@ -872,7 +966,7 @@ __global__ void __launch_bounds__(kThreads, bulk_min_ctas(CT))
 template <typename GT, bool STASH>
 __global__ void __launch_bounds__(kThreads, ZO_MULTI_MIN_CTAS)
     pass1_multi_kernel(const Pass1Args a) {
-  pdl_launch_dependents();
+  pass1_prologue();
   __shared__ double red[kThreads / 32];
   __shared__ int s_last;
   const int tid = threadIdx.x;
@@ -946,6 +1040,9 @@ template <typename GT, typename PT, int SRC, bool M16>
 __global__ void __launch_bounds__(kThreads, (M16 && SRC != 0) ? ZO_PASS2_M16_MIN_CTAS
                                                                : ZO_PASS2_MIN_CTAS)
     pass2_kernel(const Pass2Args a) {
+#if ZO_PDL_PASS1
+  pdl_launch_dependents();  // the next step's pass 1 may be scheduled
+#endif
   const int64_t G0 = gridDim.x;
   if (threadIdx.x == 0 && (int64_t)blockIdx.x < a.ntiles) {
     // Before the wait this overlaps the end of pass 1, so only data pass 1

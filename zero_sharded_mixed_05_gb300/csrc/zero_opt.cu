@@ -21,6 +21,12 @@
 
 #include "host_util.h"
 #include "kernels.cuh"
+
+// Preferred shared-memory carveout (percent) set on every kernel; -1 leaves
+// the driver's choice.
+#ifndef ZO_SMEM_CARVEOUT
+#define ZO_SMEM_CARVEOUT -1
+#endif
 #include "zero_opt.h"
 
 // 1: a single gradient buffer takes the bulk-copy pass 1 (pass1_bulk_kernel)
@@ -212,6 +218,11 @@ int occupancy(zero_opt_t h, const void* fn) {
   const size_t smem = dyn_smem(fn);
   if (smem > 0)
     cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+#if ZO_SMEM_CARVEOUT >= 0
+  // one shared-memory carveout for every kernel, so that consecutive
+  // launches never wait for an SM to change its L1/shared split
+  cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, ZO_SMEM_CARVEOUT);
+#endif
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, zo::kThreads, smem) != cudaSuccess ||
       n < 1)
@@ -444,7 +455,7 @@ zero_status run(zero_opt_t h, int32_t rank, const std::vector<HostRun>& runs, in
   g1 = std::min<int64_t>(g1, std::max<int64_t>(units, 1));
   g1 = std::max<int64_t>(std::min<int64_t>(g1, zo::kMaxCtas - 1), 1) + a1.scalar_cta;
   if (h->ev[0]) cudaEventRecord(h->ev[0], stream);
-  st = launch_kernel(h, f1, (int)g1, &a1, stream);
+  st = launch_kernel(h, f1, (int)g1, &a1, stream, ZO_PDL_PASS1 && h->ev[0] == nullptr);
   if (h->ev[1]) cudaEventRecord(h->ev[1], stream);
   if (st != ZERO_OK || mode == zo::kStatsOnly || plan->ntiles == 0) {
     if (h->ev[2]) cudaEventRecord(h->ev[2], stream);
