@@ -479,9 +479,6 @@ struct SqAcc {
   }
 };
 
-#ifndef ZO_BLOCKSUM_TREE
-#define ZO_BLOCKSUM_TREE 0
-#endif
 // Fixed-shape CTA sum in binary64: the result (valid in thread 0) depends only
 // on the inputs, never on timing.
 __device__ __forceinline__ double block_sum(double x, double* red) {
@@ -491,19 +488,10 @@ __device__ __forceinline__ double block_sum(double x, double* red) {
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = x;
   __syncthreads();
   double t = 0.0;
-#if ZO_BLOCKSUM_TREE
-  if (threadIdx.x < 32) {
-    t = threadIdx.x < kThreads / 32 ? red[threadIdx.x] : 0.0;
-#pragma unroll
-    for (int off = kThreads / 64; off > 0; off >>= 1)
-      t = __dadd_rn(t, __shfl_down_sync(0xffffffffu, t, off));
-  }
-#else
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int w = 0; w < kThreads / 32; ++w) t = __dadd_rn(t, red[w]);
   }
-#endif
   return t;
 }
 
@@ -637,9 +625,6 @@ static __device__ __forceinline__ void decide(const Pass1Args& a, double own_sum
 // draws the last ticket synchronizes with every earlier increment (they form
 // one release sequence), and its barrier then orders its other threads'
 // loads after all of those writes.
-#ifndef ZO_TICKET_ACQREL
-#define ZO_TICKET_ACQREL 1
-#endif
 __device__ __forceinline__ unsigned int ticket_add_acq_rel(unsigned int* p) {
   unsigned int old;
   asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
@@ -657,19 +642,11 @@ __device__ __forceinline__ void pass1_finish(const Pass1Args& a, double mine, in
   if (tid == 0) {
     a.ws->part_sumsq[blockIdx.x] = blk;
     a.ws->part_flag[blockIdx.x] = any;
-#if ZO_TICKET_ACQREL
     const unsigned int prev = ticket_add_acq_rel(&a.ws->ticket);
-#else
-    __threadfence();
-    const unsigned int prev = atomicAdd(&a.ws->ticket, 1u);
-#endif
     *s_last = (prev == gridDim.x - 1) ? 1 : 0;
   }
   __syncthreads();
   if (!*s_last) return;
-#if !ZO_TICKET_ACQREL
-  __threadfence();
-#endif
   DecideInputs in;
   if (tid == 0) in = load_decide_inputs(a);
   // each thread folds the partials c = tid, tid + 256, ... in that order; the
