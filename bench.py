@@ -588,7 +588,10 @@ def run_ours(args):
     # gradients (into a second device buffer set) and the download of step
     # i's parameters (from one of two alternating parameter buffers) run on
     # their own streams while step i+1 computes.
-    e2e_ms = e2e_pipelined(setup, stream, max(3, min(K, 50)))
+    # The host side of the box is shared, so the link-bound figure varies from
+    # run to run: the median of three repetitions is reported, with all three.
+    e2e_runs = [e2e_pipelined(setup, stream, max(3, min(K, 50))) for _ in range(3)]
+    e2e_ms = statistics.median(e2e_runs)
     if ws > 1:
         e2e_ms = max_over_ranks(e2e_ms, dev)
     e2e_value = ws * n / (e2e_ms * 1e-3)
@@ -632,8 +635,10 @@ def run_ours(args):
             "e2e": {"value": e2e_value, "unit": "params/s",
                     "h2d_bytes_per_step": setup.input_bytes(),
                     "d2h_bytes_per_step": setup.output_bytes(), "ms_per_step": e2e_ms,
+                    "ms_per_step_runs": e2e_runs,
                     "transfers": "pinned host buffers; H2D and D2H on their own streams, "
-                                 "double-buffered device copies, overlapped with the steps",
+                                 "double-buffered device copies, overlapped with the steps; "
+                                 "median of 3 repetitions",
                     "link_gbs": links},
             "gpu_launches": launches,
             "clocks": clk,
