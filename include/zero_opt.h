@@ -286,6 +286,10 @@ zero_status zero_opt_step_folded(zero_opt_t h, int32_t rank, const zero_opt_buff
  * allocation and no host synchronization; it only launches kernels on `stream`,
  * and the decision stays on the device.  Such a call can therefore be captured
  * into a CUDA graph (stream capture) and the graph replayed once per step.
+ * Both kernels are programmatic dependent launches: the first may be
+ * scheduled while the kernel before it on `stream` still runs, and waits for
+ * that kernel to complete, with all its writes visible, before it touches
+ * memory.  So a caller sees plain stream order.
  * Errors: EINVAL (h/bufs/grads NULL, a NULL state or gradient pointer for a
  * non-empty shard, R or K < 1, R*K > 1024), ERANGE (rank outside [0, world)),
  * ECUDA (no device, wrong current device, or a launch failure). */
