@@ -396,18 +396,35 @@ zero_status zero_opt_ckpt_read(const char* path, zero_opt_ckpt_info* info,
 /* Save `rank`'s shard: its DEVICE master, m and v (shard-local; the first
  * real_len elements are stored) and its loss-scaler replica.  Synchronizes
  * `stream`.  Errors: as zero_opt_ckpt_write, plus ERANGE (rank), ECUDA,
- * ENOTSUP (a master16 handle: it has no fp32 master weights to store). */
+ * ENOTSUP (a master16 handle: its masters are in param16, see
+ * zero_opt_save_shard16). */
 zero_status zero_opt_save_shard(zero_opt_t h, int32_t rank, const float* master,
                                 const float* m, const float* v, void* stream,
                                 const char* path);
+
+/* Save `rank`'s shard of a master16 handle: its DEVICE 16-bit parameters
+ * (the master weights; the full padded buffer unless param16_shard_local),
+ * m, v and its loss-scaler replica, in the same file format.  The masters
+ * are stored widened to binary32, which is exact.  zero_opt_load_shard
+ * therefore restores them bit for bit (NaN payloads included), and
+ * zero_opt_consolidate_fp32 reads the files like any other.  Synchronizes
+ * `stream`.  Errors: as zero_opt_save_shard, plus EINVAL (a handle without
+ * master16). */
+zero_status zero_opt_save_shard16(zero_opt_t h, int32_t rank, const void* param16,
+                                  int32_t param16_shard_local, const float* m, const float* v,
+                                  void* stream, const char* path);
 
 /* Resume `rank`'s shard from a file written for the same numel, world and
  * rank: fills the DEVICE master, m and v (shard-local), restores the rank's
  * loss-scaler replica and, when param16 is non-NULL, rewrites the rank's
  * slice of the 16-bit parameter copy as the rounding of the restored master
  * weights (param16 is the full padded buffer unless param16_shard_local).
+ * For a master16 handle `master` is not used and param16 is required: the
+ * file's masters are written into param16.  That is exact for a file from
+ * zero_opt_save_shard16; for a file of fp32 masters it rounds them to
+ * nearest even.
  * Synchronizes `stream`.  Errors: EINVAL (file for another numel/world/rank,
- * unreadable or corrupt file), ERANGE, ECUDA, ENOTSUP (a master16 handle). */
+ * unreadable or corrupt file, a NULL buffer), ERANGE, ECUDA. */
 zero_status zero_opt_load_shard(zero_opt_t h, int32_t rank, float* master, float* m,
                                 float* v, void* param16, int32_t param16_shard_local,
                                 void* stream, const char* path);

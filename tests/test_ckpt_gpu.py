@@ -97,19 +97,156 @@ def test_save_load_resume_is_bit_exact(tmp_path):
     z.zero_opt_destroy(h3)
 
 
-def test_master16_handles_have_no_shard_files(tmp_path):
-    """A master16 handle keeps no fp32 masters, so shard files (which hold
-    them) are refused with ZERO_ENOTSUP before any work."""
+def _m16_grads(numel, P, dt, n, dev):
+    import torch
+    kind = synth.F16 if dt == torch.float16 else synth.BF16
+    out = []
+    for s in range(n):
+        g = torch.zeros(P, dtype=dt, device=dev)
+        g[:numel] = synth.normal_torch(11, 1, numel, 0.3, kind, device=dev, offset=s * numel)
+        out.append(g)
+    return out
+
+
+@pytest.mark.parametrize("code", [O.BF16, O.FP16], ids=["bf16", "fp16"])
+def test_master16_save_load_resume_is_bit_exact(tmp_path, code):
+    """Low-precision masters: the 16-bit parameters are the masters, saved
+    widened to binary32 (zero_opt_save_shard16) and restored into the 16-bit
+    buffer by zero_opt_load_shard.  Eight steps straight equal four steps, a
+    save of both ranks' shards, a load into fresh buffers and a fresh handle,
+    and four more steps, bit for bit; consolidation gives the widened
+    masters."""
     import torch
 
     import zero_sharded_mixed_05_gb300 as z
-    cfg = z.make_config(numel=1000, world=1, grad_dtype=z.BF16, master16=True)
+    dev = torch.device("cuda:0")
+    dt = torch.float16 if code == O.FP16 else torch.bfloat16
+    numel, world = 200_003, 2
+    cfg = z.make_config(numel=numel, world=world, grad_dtype=code, lr=1e-3,
+                        weight_decay=0.01, max_grad_norm=0.5, dynamic_scale=True,
+                        init_scale=64.0, scale_window=3, master16=True)
+    _, _, S, P = O.shard_bounds(numel, world, 0)
+    q0 = O.f32_to_16(synth.normal_np(12, 0, 0, numel, 0.02, synth.F32), code)
+    grads = _m16_grads(numel, P, dt, 8, dev)
+
+    def fresh():
+        p16 = torch.zeros(P, dtype=dt, device=dev)
+        p16[:numel] = torch.from_numpy(q0.view(np.int16).copy()).view(dt).to(dev)
+        return [[torch.zeros(S, device=dev), torch.zeros(S, device=dev)]
+                for _ in range(world)], p16
+
+    def steps(h, mv, p16, lo, hi):
+        for s in range(lo, hi):
+            bufs = [z.make_buffers(None, *mv[r], p16, [grads[s]]) for r in range(world)]
+            G = z.zero_opt_fold_stats([z.zero_opt_grad_stats(h, r, bufs[r]) for r in range(world)])
+            for r in range(world):
+                z.zero_opt_step(h, r, bufs[r], global_stats=G)
+
+    h1 = z.zero_opt_create(cfg)
+    a, a16 = fresh()
+    steps(h1, a, a16, 0, 8)
+    h2 = z.zero_opt_create(cfg)
+    b, b16 = fresh()
+    steps(h2, b, b16, 0, 4)
+    paths = [str(tmp_path / f"m16_rank{r}.bin") for r in range(world)]
+    for r in range(world):
+        z.zero_opt_save_shard16(h2, r, b16, *b[r], paths[r])
+    # consolidation: the full masters, widened exactly
+    full = z.zero_opt_consolidate_fp32(paths, numel)
+    assert (full.view(np.uint32) == O.f16_to_f32(to_np16(b16[:numel]), code).view(np.uint32)).all()
+    z.zero_opt_destroy(h2)
+    h3 = z.zero_opt_create(cfg)
+    c, c16 = fresh()
+    c16.fill_(3.0)                              # garbage the load must overwrite
+    for x in c:
+        for t in x:
+            t.fill_(7.0)
+    for r in range(world):
+        z.zero_opt_load_shard(h3, r, None, *c[r], paths[r], param16=c16)
+    torch.cuda.synchronize()
+    assert torch.equal(b16[:numel].view(torch.int16), c16[:numel].view(torch.int16))
+    steps(h3, c, c16, 4, 8)
+    torch.cuda.synchronize()
+    for r in range(world):
+        bb, e, _, _ = O.shard_bounds(numel, world, r)
+        for x, y in zip(a[r], c[r]):
+            assert torch.equal(x[:e - bb].view(torch.int32), y[:e - bb].view(torch.int32))
+        assert z.zero_opt_loss_scale(h1, r).as_tuple() == z.zero_opt_loss_scale(h3, r).as_tuple()
+    assert torch.equal(a16[:numel].view(torch.int16), c16[:numel].view(torch.int16))
+    z.zero_opt_destroy(h1)
+    z.zero_opt_destroy(h3)
+
+
+@pytest.mark.parametrize("code", [O.BF16, O.FP16], ids=["bf16", "fp16"])
+def test_master16_shard_file_round_trips_every_pattern(tmp_path, code):
+    """All 65536 16-bit patterns as masters (zeros, subnormals, infinities,
+    NaNs with their payloads) come back bit for bit through a shard file."""
+    import torch
+
+    import zero_sharded_mixed_05_gb300 as z
+    dev = torch.device("cuda:0")
+    dt = torch.float16 if code == O.FP16 else torch.bfloat16
+    n = 65536
+    cfg = z.make_config(numel=n, world=1, grad_dtype=code, master16=True)
     h = z.zero_opt_create(cfg)
-    t = torch.zeros(1000, device="cuda:0")
-    with pytest.raises(z.ZeroOptError) as e:
-        z.zero_opt_save_shard(h, 0, None, t, t, str(tmp_path / "x.zshard"))
-    assert e.value.status == z.ZERO_ENOTSUP
-    with pytest.raises(z.ZeroOptError) as e:
-        z.zero_opt_load_shard(h, 0, None, t, t, str(tmp_path / "x.zshard"))
-    assert e.value.status == z.ZERO_ENOTSUP
+    pats = torch.arange(n, dtype=torch.int32).to(torch.int16).view(dt).to(dev)
+    m = torch.from_numpy(synth.normal_np(13, 0, 0, n, 1e-3, synth.F32)).to(dev)
+    v = torch.from_numpy(np.abs(synth.normal_np(13, 1, 0, n, 1e-6, synth.F32))).to(dev)
+    path = str(tmp_path / "pats.bin")
+    z.zero_opt_save_shard16(h, 0, pats, m, v, path)
+    q = torch.zeros(n, dtype=dt, device=dev)
+    m2, v2 = torch.zeros_like(m), torch.zeros_like(v)
+    z.zero_opt_load_shard(h, 0, None, m2, v2, path, param16=q)
+    torch.cuda.synchronize()
+    assert torch.equal(q.view(torch.int16), pats.view(torch.int16))
+    assert torch.equal(m2.view(torch.int32), m.view(torch.int32))
+    assert torch.equal(v2.view(torch.int32), v.view(torch.int32))
     z.zero_opt_destroy(h)
+
+
+def test_fp32_shard_file_into_low_precision_masters(tmp_path):
+    """A shard file of fp32 masters loaded by a master16 handle: the 16-bit
+    masters are the fp32 values rounded to nearest even (the oracle's cast)."""
+    import torch
+
+    import zero_sharded_mixed_05_gb300 as z
+    dev = torch.device("cuda:0")
+    n = 100_003
+    p = synth.normal_np(14, 0, 0, n, 0.02, synth.F32)
+    path = str(tmp_path / "fp32.bin")
+    hf = z.zero_opt_create(z.make_config(numel=n, world=1, grad_dtype=z.BF16))
+    t = lambda a: torch.from_numpy(a).to(dev)  # noqa: E731
+    z.zero_opt_save_shard(hf, 0, t(p), t(np.zeros(n, np.float32)), t(np.zeros(n, np.float32)), path)
+    z.zero_opt_destroy(hf)
+    h = z.zero_opt_create(z.make_config(numel=n, world=1, grad_dtype=z.BF16, master16=True))
+    q = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    m, v = torch.zeros(n, device=dev), torch.zeros(n, device=dev)
+    z.zero_opt_load_shard(h, 0, None, m, v, path, param16=q)
+    torch.cuda.synchronize()
+    assert (to_np16(q) == O.f32_to_16(p, O.BF16)).all()
+    z.zero_opt_destroy(h)
+
+
+def test_shard_file_calls_check_the_master_mode(tmp_path):
+    """zero_opt_save_shard refuses a master16 handle (its masters are the
+    16-bit parameters: ZERO_ENOTSUP), zero_opt_save_shard16 a handle with fp32
+    masters (ZERO_EINVAL), and a master16 load needs the 16-bit buffer."""
+    import torch
+
+    import zero_sharded_mixed_05_gb300 as z
+    t = torch.zeros(1000, device="cuda:0")
+    q = torch.zeros(1000, dtype=torch.bfloat16, device="cuda:0")
+    h16 = z.zero_opt_create(z.make_config(numel=1000, world=1, grad_dtype=z.BF16, master16=True))
+    h32 = z.zero_opt_create(z.make_config(numel=1000, world=1, grad_dtype=z.BF16))
+    with pytest.raises(z.ZeroOptError) as e:
+        z.zero_opt_save_shard(h16, 0, None, t, t, str(tmp_path / "x.bin"))
+    assert e.value.status == z.ZERO_ENOTSUP
+    with pytest.raises(z.ZeroOptError) as e:
+        z.zero_opt_save_shard16(h32, 0, q, t, t, str(tmp_path / "x.bin"))
+    assert e.value.status == z.ZERO_EINVAL
+    z.zero_opt_save_shard16(h16, 0, q, t, t, str(tmp_path / "y.bin"))
+    with pytest.raises(z.ZeroOptError) as e:
+        z.zero_opt_load_shard(h16, 0, None, t, t, str(tmp_path / "y.bin"))
+    assert e.value.status == z.ZERO_EINVAL
+    z.zero_opt_destroy(h16)
+    z.zero_opt_destroy(h32)

@@ -118,6 +118,7 @@ SIGNATURES = [
     ("zero_opt_ckpt_write", _i32, [ctypes.c_char_p, _P(zero_opt_ckpt_info), _vp, _vp, _vp]),
     ("zero_opt_ckpt_read", _i32, [ctypes.c_char_p, _P(zero_opt_ckpt_info), _vp, _vp, _vp]),
     ("zero_opt_save_shard", _i32, [_vp, _i32, _vp, _vp, _vp, _vp, ctypes.c_char_p]),
+    ("zero_opt_save_shard16", _i32, [_vp, _i32, _vp, _i32, _vp, _vp, _vp, ctypes.c_char_p]),
     ("zero_opt_load_shard", _i32, [_vp, _i32, _vp, _vp, _vp, _vp, _i32, _vp, ctypes.c_char_p]),
     ("zero_opt_consolidate_fp32", _i32, [_P(ctypes.c_char_p), _i32, _i64, _vp]),
     ("zero_opt_grad_stats_noalloc", _i32, [_P(_vp), _i32, _i32, _i64, _vp, _vp]),
@@ -459,6 +460,15 @@ def zero_opt_ckpt_read(path: str, with_payload: bool = True):
 def zero_opt_save_shard(h, rank: int, master, m, v, path: str, stream=None) -> None:
     _check(lib().zero_opt_save_shard(h, rank, _ptr(master), _ptr(m), _ptr(v), _stream(stream),
                                      os.fsencode(path)), "zero_opt_save_shard")
+
+
+def zero_opt_save_shard16(h, rank: int, param16, m, v, path: str,
+                          param16_shard_local: bool = False, stream=None) -> None:
+    """Shard file of a master16 handle: its 16-bit masters (widened exactly), m, v
+    and loss-scaler replica."""
+    _check(lib().zero_opt_save_shard16(h, rank, _ptr(param16), int(param16_shard_local),
+                                       _ptr(m), _ptr(v), _stream(stream), os.fsencode(path)),
+           "zero_opt_save_shard16")
 
 
 def zero_opt_load_shard(h, rank: int, master, m, v, path: str, param16=None,

@@ -13,7 +13,7 @@ CSRC = os.path.join(PKG, "csrc")
 SOURCES = [os.path.join(CSRC, "zero_opt.cu"), os.path.join(CSRC, "ckpt.cpp"),
            os.path.join(CSRC, "noalloc.cu"), os.path.join(CSRC, "host_step.cpp")]
 DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("kernels.cuh", "zero_opt_internal.h",
-                                                     "host_util.h", "decide_core.h")] + [
+                                                     "host_util.h", "decide_core.h", "host_cast.h")] + [
     os.path.join(INCLUDE, "zero_opt.h")]
 LIB = os.path.join(PKG, "libzero_opt.so")
 

@@ -20,6 +20,7 @@
 #include <vector>
 
 #include "host_util.h"
+#include "host_cast.h"
 #include "kernels.cuh"
 
 // Preferred shared-memory carveout (percent) set on every kernel; -1 leaves
@@ -907,7 +908,8 @@ zero_status zero_opt_save_shard(zero_opt_t h, int32_t rank, const float* master,
   zero_status st = check_handle_rank(h, rank);
   if (st != ZERO_OK) return st;
   if (h->cfg.master16)
-    return fail(ZERO_ENOTSUP, "shard files hold fp32 master weights; a master16 handle has none");
+    return fail(ZERO_ENOTSUP,
+                "a master16 handle keeps its masters in param16: use zero_opt_save_shard16");
   if (!path) return fail(ZERO_EINVAL, "path is NULL");
   zero_opt_ckpt_info info;
   std::memset(&info, 0, sizeof(info));
@@ -936,13 +938,52 @@ zero_status zero_opt_save_shard(zero_opt_t h, int32_t rank, const float* master,
   return zero_opt_ckpt_write(path, &info, hm.data(), hmm.data(), hv.data());
 }
 
+zero_status zero_opt_save_shard16(zero_opt_t h, int32_t rank, const void* param16,
+                                  int32_t param16_shard_local, const float* m, const float* v,
+                                  void* stream, const char* path) {
+  zero_status st = check_handle_rank(h, rank);
+  if (st != ZERO_OK) return st;
+  if (!h->cfg.master16)
+    return fail(ZERO_EINVAL, "not a master16 handle: use zero_opt_save_shard");
+  if (!path) return fail(ZERO_EINVAL, "path is NULL");
+  zero_opt_ckpt_info info;
+  std::memset(&info, 0, sizeof(info));
+  int64_t shard = 0;
+  zo::shard_range(h->cfg.numel, h->cfg.world, rank, &info.begin, &info.real_len, &shard);
+  info.numel = h->cfg.numel;
+  info.world = h->cfg.world;
+  info.rank = rank;
+  if (info.real_len > 0 && (!param16 || !m || !v))
+    return fail(ZERO_EINVAL, "param16, m and v must be non-NULL");
+  st = check_device(h);
+  if (st != ZERO_OK) return st;
+  st = zero_opt_loss_scale(h, rank, stream, &info.scaler);
+  if (st != ZERO_OK) return st;
+  const size_t n = (size_t)info.real_len;
+  std::vector<uint16_t> hq(n);
+  std::vector<float> hm(n), hmm(n), hv(n);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (n > 0) {
+    const uint16_t* q =
+        static_cast<const uint16_t*>(param16) + (param16_shard_local ? 0 : info.begin);
+    e = cudaMemcpyAsync(hq.data(), q, n * 2, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(hmm.data(), m, n * 4, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(hv.data(), v, n * 4, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "zero_opt_save_shard16");
+  const bool fp16 = h->cfg.param_dtype == ZERO_FP16;
+  for (size_t i = 0; i < n; ++i) hm[i] = zo::hc::widen16(hq[i], fp16);
+  return zero_opt_ckpt_write(path, &info, hm.data(), hmm.data(), hv.data());
+}
+
 zero_status zero_opt_load_shard(zero_opt_t h, int32_t rank, float* master, float* m,
                                 float* v, void* param16, int32_t param16_shard_local,
                                 void* stream, const char* path) {
   zero_status st = check_handle_rank(h, rank);
   if (st != ZERO_OK) return st;
-  if (h->cfg.master16)
-    return fail(ZERO_ENOTSUP, "shard files hold fp32 master weights; a master16 handle has none");
+  const bool m16 = h->cfg.master16 != 0;
   if (!path) return fail(ZERO_EINVAL, "path is NULL");
   zero_opt_ckpt_info info;
   st = zero_opt_ckpt_read(path, &info, nullptr, nullptr, nullptr);
@@ -950,25 +991,37 @@ zero_status zero_opt_load_shard(zero_opt_t h, int32_t rank, float* master, float
   if (info.numel != h->cfg.numel || info.world != h->cfg.world || info.rank != rank)
     return fail(ZERO_EINVAL, "%s was written for numel %lld, world %d, rank %d", path,
                 (long long)info.numel, info.world, info.rank);
-  if (info.real_len > 0 && (!master || !m || !v))
-    return fail(ZERO_EINVAL, "master, m and v must be non-NULL");
+  if (info.real_len > 0 && (m16 ? (!param16 || !m || !v) : (!master || !m || !v)))
+    return fail(ZERO_EINVAL, m16 ? "param16 (the masters of a master16 handle), m and v must be "
+                                   "non-NULL"
+                                 : "master, m and v must be non-NULL");
   st = check_device(h);
   if (st != ZERO_OK) return st;
   const size_t n = (size_t)info.real_len;
   std::vector<float> hm(n), hmm(n), hv(n);
   st = zero_opt_ckpt_read(path, &info, hm.data(), hmm.data(), hv.data());
   if (st != ZERO_OK) return st;
+  // 16-bit masters: the file's binary32 masters narrowed (exactly, when they
+  // were written by zero_opt_save_shard16; else rounded to nearest even)
+  std::vector<uint16_t> hq(m16 ? n : 0);
+  const bool fp16 = h->cfg.param_dtype == ZERO_FP16;
+  for (size_t i = 0; i < hq.size(); ++i) hq[i] = zo::hc::narrow16(hm[i], fp16);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
   if (n > 0) {
-    e = cudaMemcpyAsync(master, hm.data(), n * 4, cudaMemcpyHostToDevice, s);
+    if (m16) {
+      uint16_t* q = static_cast<uint16_t*>(param16) + (param16_shard_local ? 0 : info.begin);
+      e = cudaMemcpyAsync(q, hq.data(), n * 2, cudaMemcpyHostToDevice, s);
+    } else {
+      e = cudaMemcpyAsync(master, hm.data(), n * 4, cudaMemcpyHostToDevice, s);
+    }
     if (e == cudaSuccess) e = cudaMemcpyAsync(m, hmm.data(), n * 4, cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess) e = cudaMemcpyAsync(v, hv.data(), n * 4, cudaMemcpyHostToDevice, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "zero_opt_load_shard");
   st = zero_opt_set_loss_scale(h, rank, stream, &info.scaler);
   if (st != ZERO_OK) return st;
-  if (param16 && n > 0) {
+  if (!m16 && param16 && n > 0) {
     zo::CastArgs ca;
     ca.master = master;
     ca.p16 = static_cast<unsigned short*>(param16) + (param16_shard_local ? 0 : info.begin);
