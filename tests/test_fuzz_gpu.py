@@ -3,7 +3,8 @@
 Each case draws a shard layout (Ψ, N, which ranks step), the gradient buffers
 (R, K, fp16/bf16, full or shard-local, misaligned or not, stashed or not),
 the optimizer (lr, weight decay, clipping, bias correction, static or dynamic
-scale with hysteresis and a window, WarmupLR) and the master-weight mode, runs
+scale with hysteresis and a window, WarmupLR), the master-weight mode and the
+16-bit parameter type, runs
 three steps on the GPU through the C ABI and on the oracle, and requires the
 parity bar of the other tests: decisions and scaler state bit-exact, fp32
 state within 1e-6 relative, 16-bit parameters within one ulp.  The draws
@@ -58,6 +59,8 @@ def draw(seed):
         shard_local_grads=bool(rng.integers(0, 2)),
         stash=bool(ranks * micro > 4 and rng.integers(0, 2)),
         misalign=int(rng.choice([0, 0, 1, 3])), inject=inject, master16=master16)
+    # drawn last, so that the earlier fields of every seed stay as they were
+    case.pdtype = int(rng.choice([gdtype, gdtype, 1 - gdtype]))
     return case
 
 

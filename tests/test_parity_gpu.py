@@ -461,3 +461,18 @@ def test_steps_across_the_bias_correction_table(t0, warmup):
         assert (a.cpu().numpy().view(np.uint32) == b.view(np.uint32)).all()
     assert (to_np16(state[3]) == ref[3]).all()
     z.zero_opt_destroy(h)
+
+
+@pytest.mark.parametrize("ranks", [1, 2], ids=["one-buffer", "two-buffers"])
+@pytest.mark.parametrize("master16", [False, True], ids=["fp32-masters", "16-bit-masters"])
+@pytest.mark.parametrize("g,p", [(O.FP16, O.BF16), (O.BF16, O.FP16)],
+                         ids=["fp16-grads-bf16-params", "bf16-grads-fp16-params"])
+def test_mixed_16bit_types(g, p, master16, ranks):
+    """Gradients in one 16-bit type and parameters in the other (param_dtype),
+    with fp32 or 16-bit masters, over two shards with folded statistics,
+    dynamic scaling and clipping."""
+    case = FlatCase(numel=300_007, world=2, ranks=ranks, gdtype=g, pdtype=p, lr=1e-3, wd=0.01,
+                    max_norm=0.5, dynamic=True, init_scale=256.0, window=3, sigma=1e-3,
+                    steps=5, master16=master16, seed=0x5EED0D00)
+    res = run_flat(case)
+    assert_flat_parity(res)
