@@ -476,3 +476,12 @@ def test_mixed_16bit_types(g, p, master16, ranks):
                     steps=5, master16=master16, seed=0x5EED0D00)
     res = run_flat(case)
     assert_flat_parity(res)
+
+
+@pytest.mark.parametrize("master16", [False, True], ids=["fp32-masters", "16-bit-masters"])
+def test_list_with_mixed_16bit_types(master16):
+    """The per-tensor list with bf16 gradients and fp16 parameters: ragged
+    tensor sizes, two gradient buffers (the multi-buffer pass 1)."""
+    res = run_list([5000, 2049, 1, 70_001, 4096], gdtype=O.BF16, pdtype=O.FP16, lr=1e-3,
+                   wd=0.01, max_norm=0.5, steps=3, ranks=2, master16=master16)
+    assert_flat_parity(res)
