@@ -485,3 +485,45 @@ def test_list_with_mixed_16bit_types(master16):
     res = run_list([5000, 2049, 1, 70_001, 4096], gdtype=O.BF16, pdtype=O.FP16, lr=1e-3,
                    wd=0.01, max_norm=0.5, steps=3, ranks=2, master16=master16)
     assert_flat_parity(res)
+
+
+@pytest.mark.parametrize("master16", [False, True], ids=["fp32-masters", "16-bit-masters"])
+def test_state_alignment_selects_the_access_width_not_the_result(master16):
+    """Pass 2 moves the fp32 state with 256-bit accesses when master, m and v
+    are 32-byte aligned and with 128-bit ones when they are only 16-byte
+    aligned.  The same three steps on both layouts give bit-identical state."""
+    import torch
+
+    import zero_sharded_mixed_05_gb300 as z
+    dev = torch.device("cuda:0")
+    n = 300_007
+    cfg = z.make_config(numel=n, world=1, grad_dtype=z.BF16, lr=1e-3, weight_decay=0.01,
+                        max_grad_norm=0.5, dynamic_scale=False, init_scale=1.0,
+                        master16=master16)
+    p0 = synth.normal_np(0x5EED0E00, 0, 0, n, 0.02, synth.F32)
+    q0 = O.f32_to_16(p0, O.BF16)
+    grads = [synth.normal_torch(0x5EED0E00, 1, n, 1e-2, synth.BF16, device=dev, offset=s * n)
+             for s in range(3)]
+
+    def run(shift):
+        # fp32 arrays at `shift` floats past a 512-byte aligned allocation
+        arrs = [torch.zeros(n + 8, device=dev)[shift:shift + n] for _ in range(3)]
+        arrs[0].copy_(torch.from_numpy(p0))
+        p16 = torch.from_numpy(q0.view(np.int16).copy()).view(torch.bfloat16).to(dev)
+        h = z.zero_opt_create(cfg)
+        for g in grads:
+            z.zero_opt_step(h, 0, z.make_buffers(None if master16 else arrs[0], arrs[1],
+                                                 arrs[2], p16, [g]))
+        torch.cuda.synchronize()
+        z.zero_opt_destroy(h)
+        return [a.clone() for a in arrs], p16.clone()
+
+    (a, ap), (b, bp) = run(0), run(4)
+    assert arrs_equal(a, b, master16)
+    assert torch.equal(ap.view(torch.int16), bp.view(torch.int16))
+
+
+def arrs_equal(a, b, master16):
+    import torch
+    first = 1 if master16 else 0         # the master array is unused with 16-bit masters
+    return all(torch.equal(x.view(torch.int32), y.view(torch.int32)) for x, y in zip(a[first:], b[first:]))

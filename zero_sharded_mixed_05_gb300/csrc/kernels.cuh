@@ -1006,6 +1006,20 @@ __device__ __forceinline__ void adam_elem(float sj, float& p, float& m, float& v
   p = __fsub_rn(p, __fmul_rn(c.step_size, __fdiv_rn(m, den)));
 }
 
+// Eight floats at a 32-byte aligned address, as one 256-bit access with the
+// streaming cache hint.
+__device__ __forceinline__ void ld8cs(const float* p, float* d) {
+  asm volatile("ld.global.cs.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3]), "=f"(d[4]), "=f"(d[5]),
+                 "=f"(d[6]), "=f"(d[7])
+               : "l"(p));
+}
+__device__ __forceinline__ void st8cs(float* p, const float* d) {
+  asm volatile("st.global.cs.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(d[0]),
+               "f"(d[1]), "f"(d[2]), "f"(d[3]), "f"(d[4]), "f"(d[5]), "f"(d[6]), "f"(d[7])
+               : "memory");
+}
+
 __device__ __forceinline__ void f4_to(const float4& a, float* d) {
   d[0] = a.x; d[1] = a.y; d[2] = a.z; d[3] = a.w;
 }
@@ -1092,32 +1106,50 @@ __global__ void __launch_bounds__(kThreads, (M16 && SRC != 0) ? ZO_PASS2_M16_MIN
         }
       }
       unsigned short* p16 = static_cast<unsigned short*>(s.p16) + e0;
+      // 256-bit accesses to the fp32 state when its arrays are 32-byte aligned
+      // at this tile (a property of the run, the same for every thread)
+      const bool w8 = ((((uintptr_t)(s.m + e0)) | ((uintptr_t)(s.v + e0)) |
+                        (M16 ? (uintptr_t)0 : (uintptr_t)(s.master + e0))) &
+                       31) == 0;
       if (M16) {
         Fmt<PT>::dec8(__ldcs(reinterpret_cast<const uint4*>(p16)), p);
+      } else if (w8) {
+        ld8cs(s.master + e0, p);
       } else {
         const float4* pm = reinterpret_cast<const float4*>(s.master + e0);
         f4_to(__ldcs(pm), p);
         f4_to(__ldcs(pm + 1), p + 4);
       }
-      const float4* mm = reinterpret_cast<const float4*>(s.m + e0);
-      const float4* vm = reinterpret_cast<const float4*>(s.v + e0);
-      f4_to(__ldcs(mm), m);
-      f4_to(__ldcs(mm + 1), m + 4);
-      f4_to(__ldcs(vm), v);
-      f4_to(__ldcs(vm + 1), v + 4);
+      if (w8) {
+        ld8cs(s.m + e0, m);
+        ld8cs(s.v + e0, v);
+      } else {
+        const float4* mm = reinterpret_cast<const float4*>(s.m + e0);
+        const float4* vm = reinterpret_cast<const float4*>(s.v + e0);
+        f4_to(__ldcs(mm), m);
+        f4_to(__ldcs(mm + 1), m + 4);
+        f4_to(__ldcs(vm), v);
+        f4_to(__ldcs(vm + 1), v + 4);
+      }
 #pragma unroll
       for (int i = 0; i < kVec; ++i) adam_elem(x[i], p[i], m[i], v[i], c);
-      if (!M16) {
-        float4* po = reinterpret_cast<float4*>(s.master + e0);
-        __stcs(po, make_float4(p[0], p[1], p[2], p[3]));
-        __stcs(po + 1, make_float4(p[4], p[5], p[6], p[7]));
+      if (w8) {
+        if (!M16) st8cs(s.master + e0, p);
+        st8cs(s.m + e0, m);
+        st8cs(s.v + e0, v);
+      } else {
+        if (!M16) {
+          float4* po = reinterpret_cast<float4*>(s.master + e0);
+          __stcs(po, make_float4(p[0], p[1], p[2], p[3]));
+          __stcs(po + 1, make_float4(p[4], p[5], p[6], p[7]));
+        }
+        float4* mo = reinterpret_cast<float4*>(s.m + e0);
+        float4* vo = reinterpret_cast<float4*>(s.v + e0);
+        __stcs(mo, make_float4(m[0], m[1], m[2], m[3]));
+        __stcs(mo + 1, make_float4(m[4], m[5], m[6], m[7]));
+        __stcs(vo, make_float4(v[0], v[1], v[2], v[3]));
+        __stcs(vo + 1, make_float4(v[4], v[5], v[6], v[7]));
       }
-      float4* mo = reinterpret_cast<float4*>(s.m + e0);
-      float4* vo = reinterpret_cast<float4*>(s.v + e0);
-      __stcs(mo, make_float4(m[0], m[1], m[2], m[3]));
-      __stcs(mo + 1, make_float4(m[4], m[5], m[6], m[7]));
-      __stcs(vo, make_float4(v[0], v[1], v[2], v[3]));
-      __stcs(vo + 1, make_float4(v[4], v[5], v[6], v[7]));
       __stcs(reinterpret_cast<uint4*>(p16), Fmt<PT>::enc8(p));
     } else {
 #pragma unroll
