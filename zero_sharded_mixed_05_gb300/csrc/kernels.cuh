@@ -231,6 +231,10 @@ __device__ __forceinline__ void pass1_prologue() {
   pdl_wait();
 #endif
 }
+// Return the 128-byte L2 line at `p` (128-byte aligned) to evict_normal.
+__device__ __forceinline__ void l2_normal(const void* p) {
+  asm volatile("applypriority.global.L2::evict_normal [%0], 128;" ::"l"(p) : "memory");
+}
 // Warm L2 with `bytes` at `p` (16-byte aligned, a multiple of 16 bytes).
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
@@ -789,6 +793,17 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
 }
+// The same copy with an L2 evict_last policy on the lines it reads.
+__device__ __forceinline__ void bulk_load_keep(void* dst, const void* src, uint32_t bytes,
+                                               unsigned long long* bar) {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+      : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(unsigned long long* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -869,9 +884,14 @@ __global__ void __launch_bounds__(kThreads, bulk_min_ctas(CT))
     s_whole[i % S] = whole ? 1 : 0;
     if (whole) {
       mbar_arrive_expect_tx(b, kChunkTiles * kTile * 2);
-      bulk_load(&stage_buf[(i % S) * kChunkTiles * kThreads],
-                grad_ptr(a.gptrs, c.s, 0) + (t0 - c.s.tile0) * kTile,
-                kChunkTiles * kTile * 2, b);
+      if (t0 >= a.keep_tile0)
+        bulk_load_keep(&stage_buf[(i % S) * kChunkTiles * kThreads],
+                       grad_ptr(a.gptrs, c.s, 0) + (t0 - c.s.tile0) * kTile,
+                       kChunkTiles * kTile * 2, b);
+      else
+        bulk_load(&stage_buf[(i % S) * kChunkTiles * kThreads],
+                  grad_ptr(a.gptrs, c.s, 0) + (t0 - c.s.tile0) * kTile,
+                  kChunkTiles * kTile * 2, b);
     } else {
       mbar_arrive(b);
     }
@@ -1053,7 +1073,19 @@ __global__ void __launch_bounds__(kThreads, (M16 && SRC != 0) ? ZO_PASS2_M16_MIN
   }
   pdl_wait();
   const Decision* dp = a.dec;
-  if (dp->skip) return;
+  if (dp->skip) {
+    // nothing is updated; the gradient lines pass 1 kept in L2 go back to
+    // evict_normal all the same (one lane per 128-byte line)
+    if (SRC == 1 && a.keep_tile0 < a.ntiles && (threadIdx.x & 7) == 0) {
+      RunCursor cur;
+      for (int64_t tile = a.keep_tile0 + blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
+        cur.seek(a.segs, a.nseg, tile);
+        const int64_t e0 = (tile - cur.s.tile0) * kTile + threadIdx.x * kVec;
+        if (cur.s.vec && e0 + kVec <= cur.s.n) l2_normal(grad_ptr(a.gptrs, cur.s, 0) + e0);
+      }
+    }
+    return;
+  }
   Scalars c;
   c.coef = dp->coef;
   c.b1 = dp->b1;
@@ -1082,7 +1114,9 @@ __global__ void __launch_bounds__(kThreads, (M16 && SRC != 0) ? ZO_PASS2_M16_MIN
         f4_to(__ldcs(st), x);
         f4_to(__ldcs(st + 1), x + 4);
       } else if (SRC == 1) {
-        Fmt<GT>::dec8(__ldcs(reinterpret_cast<const uint4*>(grad_ptr(a.gptrs, s, 0) + e0)), x);
+        const unsigned short* gp = grad_ptr(a.gptrs, s, 0) + e0;
+        Fmt<GT>::dec8(__ldcs(reinterpret_cast<const uint4*>(gp)), x);
+        if (tile >= a.keep_tile0 && (tid & 7) == 0) l2_normal(gp);
 #pragma unroll
         for (int i = 0; i < kVec; ++i) x[i] = __fadd_rn(0.0f, x[i]);
       } else {

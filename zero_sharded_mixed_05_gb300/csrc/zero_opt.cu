@@ -23,6 +23,12 @@
 #include "host_cast.h"
 #include "kernels.cuh"
 
+// Bytes of gradients at the top of a single buffer that pass 1 reads with an
+// L2 evict_last policy for pass 2 (0: none).
+#ifndef ZO_L2_KEEP_BYTES
+#define ZO_L2_KEEP_BYTES (64ll << 20)
+#endif
+
 // Preferred shared-memory carveout (percent) set on every kernel; -1 leaves
 // the driver's choice.
 #ifndef ZO_SMEM_CARVEOUT
@@ -438,6 +444,17 @@ zero_status run(zero_opt_t h, int32_t rank, const std::vector<HostRun>& runs, in
   a1.bc_table = h->bc_table;
   a1.inject_wait_fault = h->inject_wait_fault;
   h->inject_wait_fault = 0;
+  // The gradients pass 2 reads first (the top of a single buffer, where its
+  // reverse walk starts) are read by pass 1 with an L2 evict_last policy, up
+  // to ZO_L2_KEEP_BYTES; pass 2 returns their lines to evict_normal.  Only for
+  // steps over one 128-byte aligned run of one buffer.
+  a1.keep_tile0 = plan->ntiles;
+  if (ZO_L2_KEEP_BYTES > 0 && mode != zo::kStatsOnly && a1.ntiles > 0 && nbuf == 1 &&
+      use_stash == nullptr && runs.size() == 1 &&
+      (reinterpret_cast<uintptr_t>(runs[0].g[0]) & 127) == 0) {
+    const int64_t keep = (int64_t)ZO_L2_KEEP_BYTES / (zo::kTile * 2);
+    a1.keep_tile0 = std::max<int64_t>(0, plan->ntiles - keep);
+  }
 
   const void* f1 = reinterpret_cast<const void*>(
       pick_pass1(h->cfg.grad_dtype, use_stash != nullptr, nbuf == 1, plan->ntiles));
@@ -472,6 +489,7 @@ zero_status run(zero_opt_t h, int32_t rank, const std::vector<HostRun>& runs, in
   a2.ntiles = plan->ntiles;
   a2.stash = use_stash;
   a2.dec = &h->ws->dec;
+  a2.keep_tile0 = a1.keep_tile0;
   const int src = use_stash ? -1 : (nbuf == 1 ? 1 : 0);
   const void* f2 = reinterpret_cast<const void*>(
       pick_pass2(h->cfg.grad_dtype, h->cfg.param_dtype, src, h->cfg.master16 != 0));

@@ -119,6 +119,8 @@ struct Pass1Args {
   zero_opt_stats* stats_out;   // kStatsOnly: also written here (device), or NULL
   int32_t g_n;
   int32_t pad3;
+  int64_t keep_tile0;          // single-buffer chunks from this tile on are read
+                               // with an L2 evict_last policy (ntiles: none)
 };
 
 struct Pass2Args {
@@ -129,6 +131,8 @@ struct Pass2Args {
   int64_t ntiles;
   const float* stash;    // non-NULL: read the reduced sums from here
   const Decision* dec;
+  int64_t keep_tile0;    // gradients of tiles from here on were kept in L2 by
+                         // pass 1; pass 2 returns their lines to evict_normal
 };
 
 }  // namespace zo
