@@ -1,16 +1,21 @@
 """Throughput of the per-shard mixed-precision ZeRO optimizer step on GB300.
 
-Default workload: a GPT-2-small-sized flat buffer of 124,439,808 parameters,
-N = 1 (unsharded, DDP-equivalent), bf16 gradients ~N(0, 1e-2), AdamW lr 3e-4
-wd 0.01, global L2 clip 1.0, no loss scaling.  Inputs are synthetic and seeded
-and are resident in HBM before the timed region; they are larger than L2
-(3.5 GB of algorithmic traffic per step), so no L2 flush is needed.
+Default workload: the per-tensor (non-flat, multi-tensor-apply) list of the
+Llama-3-8B shapes -- the 128256x4096 embedding plus 8 decoder layers (q 4096x4096,
+k/v 1024x4096, o 4096x4096, gate/up 14336x4096, down 4096x14336, two 4096
+RMSNorm weights): 73 tensors, 2,270,232,576 parameters, bf16 gradients
+~N(0, 1e-3), fp32 masters ~N(0, 0.02), AdamW lr 1e-4 wd 0.1, global L2 clip
+1.0.  It is the largest workload that fits one GPU (36 GB of state and
+gradients, 63.6 GB of algorithmic traffic per step).  Inputs are synthetic and
+seeded and are resident in HBM before the timed region; they are far larger
+than L2, so no L2 flush is needed.
 
-One "step" is one call of zero_opt_step: pass 1 (reduce, overflow flag, sum of
-squares, decision) and pass 2 (unscale, clip, AdamW, 16-bit copy).
+One "step" is one call of zero_opt_step (zero_opt_step_tensors for the list):
+pass 1 (reduce, overflow flag, sum of squares, decision) and pass 2 (unscale,
+clip, AdamW, 16-bit copy).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload gpt2|llama|fused|pertensor]
+                  [--workload pertensor|gpt2|gpt2_master16|llama|fused]
 
 Prints one JSON line (rank 0).  Under torchrun every rank runs its own copy of
 the workload on its own GPU (weak scaling) and the timing is the maximum over
@@ -49,8 +54,10 @@ def load_peaks():
 
 # ---------------------------------------------------------------- workloads
 
-def llama_shapes():
-    H, KV, F, V = 4096, 1024, 14336, 128256
+def llama_shapes(div=1):
+    """Embedding plus 8 decoder layers of Llama-3-8B; every dimension divided
+    by `div` for scaled-down profiling captures (1: the workload itself)."""
+    H, KV, F, V = 4096 // div, 1024 // div, 14336 // div, 128256 // div
     shapes = [(V, H)]
     for _ in range(8):
         shapes += [(H, H), (KV, H), (KV, H), (H, H), (F, H), (F, H), (H, F), (H,), (H,)]
@@ -86,28 +93,38 @@ WORKLOADS = {
 }
 
 
-PASS2_PROFILE = os.path.join(ROOT, "profiles", "pass2_kernel_gpt2_100M_ncu_full.md")
+# Committed ncu summaries of one pass-2 launch per workload, from which the
+# per-parameter DRAM traffic is read (scaled to the workload by its parameter
+# count: the kernel streams, so its traffic is proportional to the elements).
+PASS2_PROFILES = {
+    "gpt2": "pass2_kernel_gpt2_100M_ncu_full.md",
+    "pertensor": "pass2_kernel_pertensor_div4_ncu_full.md",
+}
 
 
-def pass2_traffic_per_param():
-    """DRAM bytes per parameter of one pass-2 launch from the committed ncu
-    summary, or None when the pass-2 kernel source changed since the capture."""
+def pass2_traffic_per_param(workload):
+    """(DRAM bytes per parameter of one pass-2 launch, profile file) from the
+    committed ncu summary of this workload, or (None, None) when there is none
+    or the pass-2 kernel source changed since the capture."""
     import hashlib
     import re
+    name = PASS2_PROFILES.get(workload)
+    if name is None:
+        return None, None
     try:
-        prof = open(PASS2_PROFILE).read()
+        prof = open(os.path.join(ROOT, "profiles", name)).read()
         src = open(os.path.join(ROOT, "zero_sharded_mixed_05_gb300", "csrc", "kernels.cuh")).read()
     except OSError:
-        return None
+        return None, None
     a = src.find("// ------------------------------------------------------------- pass 2")
     b = src.find("// ------------------------------------------------------------- 16-bit copy")
     mt = re.search(r"traffic_bytes_per_param: ([0-9.]+)", prof)
     mh = re.search(r"pass2_source_sha256: ([0-9a-f]{64})", prof)
     if a < 0 or b < 0 or not mt or not mh:
-        return None
+        return None, None
     if hashlib.sha256(src[a:b].encode()).hexdigest() != mh.group(1):
-        return None
-    return float(mt.group(1))
+        return None, None
+    return float(mt.group(1)), "profiles/" + name
 
 
 def state_bytes_per_param(w):
@@ -148,7 +165,7 @@ class Setup:
         nb = w["R"] * w["K"]
         self.stash = None
         if name == "pertensor":
-            shapes = llama_shapes()
+            shapes = llama_shapes(w.get("div", 1))
             self.items, off = [], 0
             for shp in shapes:
                 n = int(np.prod(shp))
@@ -590,19 +607,29 @@ def run_ours(args):
     # their own streams while step i+1 computes.
     # The host side of the box is shared, so the link-bound figure varies from
     # run to run: the median of three repetitions is reported, with all three.
-    e2e_runs = [e2e_pipelined(setup, stream, max(3, min(K, 50))) for _ in range(3)]
-    e2e_ms = statistics.median(e2e_runs)
-    if ws > 1:
-        e2e_ms = max_over_ranks(e2e_ms, dev)
-    e2e_value = ws * n / (e2e_ms * 1e-3)
-    links = link_rates(setup)
-    d2d = d2d_copy_gbs(dev)
+    e2e = None
+    if not args.no_e2e:
+        e2e_runs = [e2e_pipelined(setup, stream, max(3, min(K, 50))) for _ in range(3)]
+        e2e_ms = statistics.median(e2e_runs)
+        if ws > 1:
+            e2e_ms = max_over_ranks(e2e_ms, dev)
+        e2e = {"value": ws * n / (e2e_ms * 1e-3), "unit": "params/s",
+               "h2d_bytes_per_step": setup.input_bytes(),
+               "d2h_bytes_per_step": setup.output_bytes(), "ms_per_step": e2e_ms,
+               "ms_per_step_runs": e2e_runs,
+               "transfers": "pinned host buffers; H2D and D2H on their own streams, "
+                            "double-buffered device copies, overlapped with the steps; "
+                            "median of 3 repetitions",
+               "link_gbs": link_rates(setup)}
+    d2d = d2d_copy_gbs(dev) if not args.no_e2e else None
 
-    tpp = pass2_traffic_per_param() if (args.workload == "gpt2" and not stash) else None
+    tpp, tsrc = pass2_traffic_per_param(args.workload) if not stash else (None, None)
+    if w.get("div", 1) != 1 or args.numel:
+        tpp = None                    # a resized workload has no committed capture
     traffic = tpp * n if tpp is not None else None
-    traffic_src = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one pass-2 launch at "
-                   "100M parameters, scaled to this shard by parameter count "
-                   "(profiles/pass2_kernel_gpt2_100M_ncu_full.md)" if traffic is not None else None)
+    traffic_src = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one pass-2 launch, "
+                   "per parameter, scaled to this workload by parameter count (%s)" % tsrc
+                   if traffic is not None else None)
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -632,14 +659,7 @@ def run_ours(args):
                          "launches_timed": len(sampled),
                          "timing": "CUDA events around each pass on every %d-th timed "
                                    "step" % EVERY},
-            "e2e": {"value": e2e_value, "unit": "params/s",
-                    "h2d_bytes_per_step": setup.input_bytes(),
-                    "d2h_bytes_per_step": setup.output_bytes(), "ms_per_step": e2e_ms,
-                    "ms_per_step_runs": e2e_runs,
-                    "transfers": "pinned host buffers; H2D and D2H on their own streams, "
-                                 "double-buffered device copies, overlapped with the steps; "
-                                 "median of 3 repetitions",
-                    "link_gbs": links},
+            "e2e": e2e,
             "gpu_launches": launches,
             "clocks": clk,
         }
@@ -780,11 +800,15 @@ def main():
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="gpt2")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="pertensor")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--numel", type=int, default=0,
                     help="override the flat workload's parameters per shard (profiling runs)")
+    ap.add_argument("--div", type=int, default=1,
+                    help="divide every dimension of the per-tensor list by this (profiling runs)")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="leave out the end-to-end and copy-ceiling legs (profiling runs)")
     ap.add_argument("--zero2", action="store_true",
                     help="time the ZeRO-2 step with its collectives over the process group")
     ap.add_argument("--offload", action="store_true",
@@ -801,6 +825,14 @@ def main():
         w["numel"] = args.numel * w["world"]
         w["desc"] = w["desc"] + f" [resized to {args.numel:,} params per shard]"
         WORKLOADS[args.workload] = w
+    if args.div != 1:
+        if args.workload != "pertensor" or args.div < 1:
+            ap.error("--div applies to the per-tensor list and must be >= 1")
+        w = dict(WORKLOADS["pertensor"])
+        w["div"] = args.div
+        w["numel"] = int(sum(np.prod(shp) for shp in llama_shapes(args.div)))
+        w["desc"] = w["desc"] + f" [every dimension divided by {args.div}: {w['numel']:,} params]"
+        WORKLOADS["pertensor"] = w
     if args.impl == "reference":
         return run_reference(args)
     if args.offload:
