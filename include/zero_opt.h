@@ -39,7 +39,11 @@
  *     buffers must stay valid until the stream has passed the work that uses
  *     them.  The handle owns a small device workspace (about 1.1 MB: the
  *     pass-1 partials and decision, the scaler replicas and a table of the
- *     Adam bias corrections of the first 65536 steps).
+ *     Adam bias corrections of the first 65536 steps) and its run-table
+ *     arena (1 MiB of device memory and 1 MiB of page-locked host memory by
+ *     default, zero_opt_config.table_kib), all allocated by zero_opt_create
+ *     and freed by zero_opt_destroy; no other call allocates or frees device
+ *     or page-locked memory (zero_opt_get_counters counts any that would).
  *   - `stream` is a cudaStream_t (NULL is the legacy default stream).  Work is
  *     enqueued asynchronously unless the function says it synchronizes.
  *   - Calls on one handle must be ordered (one stream, or externally
@@ -105,7 +109,15 @@ typedef struct zero_opt_config {
                                widened to fp32 for the update and stored back
                                rounded to nearest even ("LLM-train tutorials
                                ch01" §1.7).  0: fp32 master (default)        */
-  int32_t reserved;         /* 0                                            */
+  int32_t table_kib;        /* KiB of the handle's run-table arena (device
+                               memory plus a page-locked host mirror of the
+                               same size), allocated by zero_opt_create;
+                               0 selects 1024.  A step's table takes 72 bytes
+                               per run (the shard, or one tensor of a list)
+                               plus 8 per run and gradient buffer, rounded up
+                               to 256; 1024 KiB holds the table of a list of
+                               13,000 tensors with one gradient buffer
+                               each.  0..2^20                               */
 } zero_opt_config;
 
 /*
@@ -281,18 +293,33 @@ zero_status zero_opt_step_folded(zero_opt_t h, int32_t rank, const zero_opt_buff
  * update's learning rate (lr, or the WarmupLR value) and after scale_window
  * consecutive applied steps the scale is multiplied by scale_factor
  * ("DeepSpeed tutorial" §2.2, §2.4, §3.2).
- * The first call with a given set of buffers builds and uploads a small run
- * table (one cudaMalloc, cached by content).  After that, a call makes no
- * allocation and no host synchronization; it only launches kernels on `stream`,
- * and the decision stays on the device.  Such a call can therefore be captured
- * into a CUDA graph (stream capture) and the graph replayed once per step.
+ * Run tables: each call describes its buffers to the kernels in a small
+ * table (72 bytes per run plus 8 per run and gradient buffer) kept in the
+ * handle's arena.  A call whose buffers the handle has seen finds its table
+ * there; for new buffers the table is copied in, ordered on `stream`, from
+ * the arena's page-locked mirror.  Neither allocates, frees or synchronizes
+ * the device, so fresh gradient buffers every step cost only that copy.  The
+ * arena keeps up to 64 tables; the least recently used, or the ones a new
+ * table's place overlaps, are dropped, and the host waits only if the copy
+ * that filled the dropped bytes has not yet run (a host more than a whole
+ * arena of new tables ahead of the device; zero_opt_get_counters counts
+ * these waits).  Dropping is safe because calls on one handle are ordered:
+ * the kernels that read a dropped table precede the copy that overwrites it.
+ * Stream capture (CUDA graphs): a call with buffers the handle has already
+ * stepped issues only its two kernel launches, with the decision on the
+ * device, so it can be captured and the graph replayed every step; its table
+ * is then kept for the life of the handle (the graph holds its address).  A
+ * call with buffers never stepped before is refused under capture (ECUDA);
+ * make one call with them first.
  * Both kernels are programmatic dependent launches: the first may be
  * scheduled while the kernel before it on `stream` still runs, and waits for
  * that kernel to complete, with all its writes visible, before it touches
  * memory.  So a caller sees plain stream order.
  * Errors: EINVAL (h/bufs/grads NULL, a NULL state or gradient pointer for a
- * non-empty shard, R or K < 1, R*K > 1024), ERANGE (rank outside [0, world)),
- * ECUDA (no device, wrong current device, or a launch failure). */
+ * non-empty shard, R or K < 1, R*K > 1024), ERANGE (rank outside [0, world);
+ * a run table larger than the arena, or no room left beside the tables
+ * that captures keep), ECUDA (no device, wrong current device, a launch
+ * failure, or new buffers under stream capture). */
 zero_status zero_opt_step(zero_opt_t h, int32_t rank, const zero_opt_buffers* bufs,
                           void* stream, const zero_opt_stats* global);
 
@@ -354,6 +381,25 @@ zero_status zero_opt_inject_wait_fault(zero_opt_t h);
 
 /* Kernels launched by this handle since creation (for launch accounting). */
 zero_status zero_opt_launch_count(zero_opt_t h, int64_t* launches);
+
+/* Accounting of a handle's launches and run tables. */
+typedef struct zero_opt_counters {
+  int64_t launches;         /* kernels launched since creation               */
+  int64_t table_uploads;    /* run tables copied into the arena              */
+  int64_t table_waits;      /* times the host waited for an earlier table
+                               copy before reusing its arena bytes           */
+  int64_t device_allocs;    /* device or page-locked allocations made after
+                               zero_opt_create returned (none by design)     */
+  int64_t device_frees;     /* frees made before zero_opt_destroy (none by
+                               design)                                       */
+  int64_t tables_cached;    /* run tables in the arena now (<= 64)           */
+  int64_t tables_pinned;    /* of those, kept for captured CUDA graphs       */
+  int64_t table_bytes;      /* size of the arena                             */
+} zero_opt_counters;
+
+/* Read the handle's counters into *out (host).  Host only.
+ * Errors: EINVAL (NULL). */
+zero_status zero_opt_get_counters(zero_opt_t h, zero_opt_counters* out);
 
 /* ---------------------------------------------------------------------------
  * Sharded checkpoints.  A DeepSpeed engine saves one checkpoint per rank and
@@ -455,10 +501,16 @@ zero_status zero_opt_consolidate_fp32(const char* const* paths, int32_t n_paths,
  * (per-CTA partial sums for at most 1024 CTAs and a completion counter),
  * held by every GPU that loads the library until the process exits.  The
  * first call on a device looks up that array's device address (with that
- * device current); make that first call before any stream capture.  Every
- * call shares the array, so calls that may overlap on the GPU (different
- * streams, or different host threads) race and must be serialized by the
- * caller.  Errors: EINVAL (NULL grads/out, a NULL gradient pointer with
+ * device current) and keeps it for the life of the process; make that first
+ * call before any stream capture, and do not use this entry point on a
+ * device after cudaDeviceReset (or any other reset of its primary context)
+ * in the same process: the kept address may then no longer name the array.
+ * Every call shares the array, so calls that may overlap on the GPU
+ * (different streams, or different host threads) race and must be
+ * serialized by the caller.  This C function sees only pointers and cannot
+ * check that each gradient buffer holds n elements of grad_dtype on the
+ * current device, or that out points at 16 writable device bytes; the
+ * caller must (the Python binding checks its tensors).  Errors: EINVAL (NULL grads/out, a NULL gradient pointer with
  * n > 0, n < 0, n_bufs < 1, bad dtype), ERANGE (n_bufs > 64), ECUDA. */
 zero_status zero_opt_grad_stats_noalloc(const void* const* grads, int32_t n_bufs,
                                         int32_t grad_dtype, int64_t n, void* stream,

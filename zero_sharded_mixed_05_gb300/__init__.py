@@ -34,7 +34,7 @@ class zero_opt_config(ctypes.Structure):
                 ("dynamic_scale", _i32), ("hysteresis", _i32),
                 ("init_scale", _f64), ("min_scale", _f64), ("scale_factor", _f64),
                 ("scale_window", _i64), ("warmup_min_lr", _f64), ("warmup_max_lr", _f64),
-                ("warmup_num_steps", _i64), ("master16", _i32), ("reserved", _i32)]
+                ("warmup_num_steps", _i64), ("master16", _i32), ("table_kib", _i32)]
 
 
 class zero_opt_buffers(ctypes.Structure):
@@ -76,6 +76,15 @@ class zero_opt_scaler_state(ctypes.Structure):
                 int(self.skipped_total), int(self.last_skipped))
 
 
+class zero_opt_counters(ctypes.Structure):
+    _fields_ = [("launches", _i64), ("table_uploads", _i64), ("table_waits", _i64),
+                ("device_allocs", _i64), ("device_frees", _i64), ("tables_cached", _i64),
+                ("tables_pinned", _i64), ("table_bytes", _i64)]
+
+    def as_dict(self):
+        return {name: int(getattr(self, name)) for name, _ in self._fields_}
+
+
 class zero_opt_ckpt_info(ctypes.Structure):
     _fields_ = [("numel", _i64), ("world", _i32), ("rank", _i32), ("begin", _i64),
                 ("real_len", _i64), ("scaler", zero_opt_scaler_state)]
@@ -115,6 +124,7 @@ SIGNATURES = [
     ("zero_opt_set_events", _i32, [_vp, _vp, _vp, _vp]),
     ("zero_opt_inject_wait_fault", _i32, [_vp]),
     ("zero_opt_launch_count", _i32, [_vp, _P(_i64)]),
+    ("zero_opt_get_counters", _i32, [_vp, _P(zero_opt_counters)]),
     ("zero_opt_ckpt_write", _i32, [ctypes.c_char_p, _P(zero_opt_ckpt_info), _vp, _vp, _vp]),
     ("zero_opt_ckpt_read", _i32, [ctypes.c_char_p, _P(zero_opt_ckpt_info), _vp, _vp, _vp]),
     ("zero_opt_save_shard", _i32, [_vp, _i32, _vp, _vp, _vp, _vp, ctypes.c_char_p]),
@@ -205,10 +215,12 @@ def make_config(numel=0, world=1, grad_dtype=FP16, param_dtype=None, lr=2e-5,
                 betas=(0.9, 0.999), eps=1e-8, weight_decay=0.01, max_grad_norm=0.0,
                 bias_correction=True, dynamic_scale=True, init_scale=65536.0,
                 min_scale=1.0, scale_factor=2.0, scale_window=1000,
-                hysteresis=1, warmup=(0.0, 0.0, 0), master16=False) -> zero_opt_config:
+                hysteresis=1, warmup=(0.0, 0.0, 0), master16=False,
+                table_kib=0) -> zero_opt_config:
     """`warmup` = (warmup_min_lr, warmup_max_lr, warmup_num_steps); 0 steps
     keeps lr constant.  `master16`: the 16-bit parameters are the master
-    weights (no fp32 master array)."""
+    weights (no fp32 master array).  `table_kib`: KiB of the handle's
+    run-table arena (0: 1024)."""
     cfg = zero_opt_config()
     _check(lib().zero_opt_config_default(ctypes.byref(cfg)), "zero_opt_config_default")
     cfg.numel = numel
@@ -229,6 +241,7 @@ def make_config(numel=0, world=1, grad_dtype=FP16, param_dtype=None, lr=2e-5,
     cfg.hysteresis = hysteresis
     cfg.warmup_min_lr, cfg.warmup_max_lr, cfg.warmup_num_steps = warmup
     cfg.master16 = int(master16)
+    cfg.table_kib = int(table_kib)
     return cfg
 
 
@@ -397,6 +410,13 @@ def zero_opt_launch_count(h) -> int:
     return out.value
 
 
+def zero_opt_get_counters(h) -> zero_opt_counters:
+    """Launches, run-table uploads and waits, and allocations after creation."""
+    out = zero_opt_counters()
+    _check(lib().zero_opt_get_counters(h, ctypes.byref(out)), "zero_opt_get_counters")
+    return out
+
+
 def zero_opt_status_string(status: int) -> str:
     return lib().zero_opt_status_string(status).decode()
 
@@ -491,8 +511,33 @@ def zero_opt_consolidate_fp32(paths, numel: int):
 def zero_opt_grad_stats_noalloc(grads, grad_dtype: int, n: int, out, stream=None) -> None:
     """Statistics of the sum of `grads` (device tensors) written into `out`, a
     device buffer of at least 16 bytes holding one zero_opt_stats; allocates
-    nothing on the device."""
+    nothing on the device.
+
+    The C entry point receives bare pointers and cannot check them, so this
+    binding does: every gradient must be a contiguous CUDA tensor of the
+    current device with the dtype `grad_dtype` names and at least `n`
+    elements, and `out` a contiguous CUDA tensor of the current device of at
+    least 16 bytes.  Anything else raises ValueError before a launch."""
+    import torch
+    want = {FP16: torch.float16, BF16: torch.bfloat16}.get(grad_dtype)
+    if want is None:
+        raise ValueError(f"grad_dtype must be FP16 or BF16, not {grad_dtype}")
     grads = list(grads)
+    dev = torch.cuda.current_device()
+
+    def on_device(t):
+        return isinstance(t, torch.Tensor) and t.is_cuda and t.device.index == dev \
+            and t.is_contiguous()
+    for i, g in enumerate(grads):
+        if not on_device(g):
+            raise ValueError(f"grads[{i}] must be a contiguous CUDA tensor on device {dev}")
+        if g.dtype != want:
+            raise ValueError(f"grads[{i}] is {g.dtype}, grad_dtype names {want}")
+        if g.numel() < n:
+            raise ValueError(f"grads[{i}] holds {g.numel()} elements, fewer than n = {n}")
+    if not on_device(out) or out.numel() * out.element_size() < 16:
+        raise ValueError(f"out must be a contiguous CUDA tensor on device {dev} of at least "
+                         "16 bytes (one zero_opt_stats)")
     arr = _ptr_array(grads)
     _check(lib().zero_opt_grad_stats_noalloc(ctypes.cast(arr, _P(_vp)), len(grads), grad_dtype,
                                              n, _stream(stream), _ptr(out)),

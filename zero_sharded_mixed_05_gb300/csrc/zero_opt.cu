@@ -1,13 +1,17 @@
 // zero_opt.cu -- host side of the C ABI declared in include/zero_opt.h.
 //
 // The host code validates arguments, turns the caller's buffers into a "plan"
-// (a device table of runs: the shard of a flat buffer or the tensors of a
-// per-tensor list, each with its gradient pointers), and launches the two
-// passes of kernels.cuh on the caller's stream.  Plans are cached by content,
-// so a training loop that passes the same buffers every step uploads its table
-// once.  The loss-scaler state of every rank lives in the handle's device
-// workspace and is only advanced by the kernels, so a step never waits for the
-// host.
+// (a table of runs: the shard of a flat buffer or the tensors of a per-tensor
+// list, each with its gradient pointers), and launches the two passes of
+// kernels.cuh on the caller's stream.  Plan tables live in a device arena that
+// zero_opt_create allocates with the rest of the handle: a table is copied in
+// once (stream-ordered, from a pinned mirror of the arena) and found again by
+// content, so a training loop that passes the same buffers every step uploads
+// its table once, and one that passes new buffers every step uploads a few
+// hundred bytes per step -- in neither case does a step allocate, free or
+// synchronize.  The loss-scaler state of every rank lives in the handle's
+// device workspace and is only advanced by the kernels, so a step never waits
+// for the host.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -93,6 +97,8 @@ zero_status check_config(const zero_opt_config* c) {
   if (c->warmup_num_steps < 0 || !(c->warmup_min_lr >= 0.0) || !(c->warmup_max_lr >= 0.0))
     return fail(ZERO_EINVAL, "warm-up steps and learning rates must be >= 0");
   if (c->master16 != 0 && c->master16 != 1) return fail(ZERO_EINVAL, "master16 must be 0 or 1");
+  if (c->table_kib < 0 || c->table_kib > (1 << 20))
+    return fail(ZERO_EINVAL, "table_kib must lie in [0, 2^20]");
   return ZERO_OK;
 }
 
@@ -141,22 +147,42 @@ struct HostRun {
   std::vector<const void*> g;
 };
 
+// A run table in the handle's arena: [Seg x nseg][const void* x nseg*nbuf].
 struct Plan {
-  std::vector<unsigned char> blob;  // [Seg x nseg][const void* x nseg*nbuf]
-  void* dev = nullptr;
+  std::vector<unsigned char> blob;  // the table as uploaded (the cache key)
+  uint64_t hash = 0;                // FNV-1a of blob, checked before the bytes
+  int64_t off = -1;                 // byte offset in the arena (-1: empty table)
+  int64_t size = 0;                 // bytes reserved in the arena
   int nseg = 0;
   int nbuf = 0;
   int64_t ntiles = 0;
-  uint64_t stamp = 0;
+  uint64_t stamp = 0;               // last use (least recently used is evicted first)
+  int ev = -1;                      // the handle's event recorded after the upload
+  bool pinned = false;              // used under stream capture: never evicted
 };
 
-constexpr size_t kMaxPlans = 64;
+// Run tables kept at once (one upload event each).
+constexpr int kMaxPlans = 64;
+// Arena bytes when the configuration leaves table_kib at 0.
+constexpr int64_t kDefaultTableBytes = 1 << 20;
+// Placement granularity of tables in the arena.
+constexpr int64_t kTableAlign = 256;
+
+uint64_t fnv1a(const std::vector<unsigned char>& b) {
+  uint64_t x = 1469598103934665603ull;
+  for (unsigned char c : b) {
+    x ^= c;
+    x *= 1099511628211ull;
+  }
+  return x;
+}
 
 }  // namespace
 
 struct zero_opt_handle {
   zero_opt_config cfg;
   bool has_device = false;
+  bool created = false;  // zero_opt_create has returned: allocations are counted
   int device = -1;
   int sms = 0;
   zo::Workspace* ws = nullptr;
@@ -167,7 +193,19 @@ struct zero_opt_handle {
   uint64_t clock = 0;
   cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};  // timing hook
   int32_t inject_wait_fault = 0;                      // test hook, one launch
+  // run-table arena: device copy, page-locked host mirror, placement head
+  unsigned char* table_dev = nullptr;
+  unsigned char* table_host = nullptr;
+  int64_t table_bytes = 0;
+  int64_t table_head = 0;
+  cudaEvent_t table_ev[kMaxPlans] = {};
+  std::vector<int> free_ev;      // indices of table_ev not held by a plan
   std::vector<Plan*> plans;
+  Plan empty_plan;               // the table of a shard with no elements
+  int64_t table_uploads = 0;
+  int64_t table_waits = 0;
+  int64_t device_allocs = 0;     // allocations after creation (none by design)
+  int64_t device_frees = 0;      // frees before destruction (none by design)
   std::vector<std::pair<const void*, int>> occ;  // kernel -> CTAs per SM
   std::mutex mu;
 };
@@ -247,11 +285,98 @@ bool run_is_vec(const HostRun& r, const float* stash) {
   return true;
 }
 
+// Device allocations of a handle go through these two, so that any made after
+// zero_opt_create (none, by design) show in zero_opt_get_counters.
+cudaError_t handle_malloc(zero_opt_t h, void** p, size_t bytes) {
+  if (h->created) h->device_allocs += 1;
+  return cudaMalloc(p, bytes);
+}
+cudaError_t handle_malloc_host(zero_opt_t h, void** p, size_t bytes) {
+  if (h->created) h->device_allocs += 1;
+  return cudaMallocHost(p, bytes);
+}
+void handle_free(zero_opt_t h, void* p) {
+  if (h->created) h->device_frees += 1;
+  if (p) cudaFree(p);
+}
+void handle_free_host(zero_opt_t h, void* p) {
+  if (h->created) h->device_frees += 1;
+  if (p) cudaFreeHost(p);
+}
+
+// Make plan `p`'s arena bytes reusable: its upload must have left the pinned
+// mirror (the host is about to overwrite it).  Kernels that read its device
+// copy were enqueued before the caller's current call, which is ordered after
+// them (calls on one handle are ordered), and so is the next upload.
+zero_status retire_plan(zero_opt_t h, Plan* p) {
+  if (p->ev >= 0) {
+    cudaError_t e = cudaEventQuery(h->table_ev[p->ev]);
+    if (e == cudaErrorNotReady) {
+      h->table_waits += 1;
+      e = cudaEventSynchronize(h->table_ev[p->ev]);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "run-table upload");
+    h->free_ev.push_back(p->ev);
+  }
+  delete p;
+  return ZERO_OK;
+}
+
+zero_status evict(zero_opt_t h, std::vector<Plan*>::iterator it) {
+  Plan* p = *it;
+  h->plans.erase(it);
+  return retire_plan(h, p);
+}
+
+// Arena offset for a table of `size` bytes: from the placement head on (or
+// from 0 when it does not fit before the end), skipping tables pinned by a
+// stream capture; the tables it overlaps are evicted.
+zero_status place(zero_opt_t h, int64_t size, int64_t* out) {
+  int64_t start = h->table_head;
+  bool wrapped = false;
+  for (;;) {
+    if (start + size > h->table_bytes) {
+      if (wrapped)
+        return fail(ZERO_ERANGE,
+                    "run-table arena of %lld bytes is full: tables used under stream capture "
+                    "hold it (raise zero_opt_config.table_kib)",
+                    (long long)h->table_bytes);
+      start = 0;
+      wrapped = true;
+    }
+    int64_t skip_to = -1;
+    for (const Plan* p : h->plans)
+      if (p->pinned && p->off < start + size && start < p->off + p->size)
+        skip_to = std::max(skip_to, p->off + p->size);
+    if (skip_to < 0) break;
+    start = skip_to;
+  }
+  for (auto it = h->plans.begin(); it != h->plans.end();) {
+    Plan* p = *it;
+    if (p->off < start + size && start < p->off + p->size) {
+      zero_status st = evict(h, it);
+      if (st != ZERO_OK) return st;
+      it = h->plans.begin();   // erase invalidated the iterator; rescan
+    } else {
+      ++it;
+    }
+  }
+  h->table_head = start + size;
+  *out = start;
+  return ZERO_OK;
+}
+
 // Serialize the runs into the device table layout; find the identical table
-// in the cache or upload a new one (ordered on `stream`).
+// in the arena or copy it in (ordered on `stream`).  Under stream capture a
+// table that is found is pinned (the graph keeps its address); a new table is
+// refused there, since placing it may need a host wait.
 zero_status get_plan(zero_opt_t h, const std::vector<HostRun>& runs, int nbuf,
                      const float* stash, cudaStream_t stream, Plan** out) {
   const int nseg = (int)runs.size();
+  if (nseg == 0) {
+    *out = &h->empty_plan;
+    return ZERO_OK;
+  }
   std::vector<zo::Seg> segs(nseg);
   std::vector<const void*> gp;
   gp.reserve((size_t)nseg * nbuf);
@@ -274,48 +399,69 @@ zero_status get_plan(zero_opt_t h, const std::vector<HostRun>& runs, int nbuf,
     for (const void* g : r.g) gp.push_back(g);
   }
   std::vector<unsigned char> blob(sizeof(zo::Seg) * nseg + sizeof(void*) * gp.size());
-  if (!blob.empty()) {
-    std::memcpy(blob.data(), segs.data(), sizeof(zo::Seg) * nseg);
-    std::memcpy(blob.data() + sizeof(zo::Seg) * nseg, gp.data(), sizeof(void*) * gp.size());
-  }
+  std::memcpy(blob.data(), segs.data(), sizeof(zo::Seg) * nseg);
+  std::memcpy(blob.data() + sizeof(zo::Seg) * nseg, gp.data(), sizeof(void*) * gp.size());
+  const uint64_t hash = fnv1a(blob);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+  const bool capturing = cap != cudaStreamCaptureStatusNone;
+
   std::lock_guard<std::mutex> lock(h->mu);
   h->clock += 1;
   for (Plan* p : h->plans) {
-    if (p->nbuf == nbuf && p->nseg == nseg && p->blob == blob) {
+    if (p->hash == hash && p->nbuf == nbuf && p->nseg == nseg && p->blob == blob) {
       p->stamp = h->clock;
+      if (capturing) p->pinned = true;
       *out = p;
       return ZERO_OK;
     }
   }
-  if (h->plans.size() >= kMaxPlans) {
-    auto it = std::min_element(h->plans.begin(), h->plans.end(),
-                               [](const Plan* a, const Plan* b) { return a->stamp < b->stamp; });
-    Plan* old = *it;
-    if (old->dev) cudaFree(old->dev);  // waits for any work still reading it
-    delete old;
-    h->plans.erase(it);
+  if (capturing)
+    return fail(ZERO_ECUDA,
+                "these buffers were never stepped before the stream capture began: make one "
+                "call with them outside the capture first (it copies their run table in)");
+  const int64_t size = ((int64_t)blob.size() + kTableAlign - 1) / kTableAlign * kTableAlign;
+  if (size > h->table_bytes)
+    return fail(ZERO_ERANGE,
+                "run table of %lld bytes (%d runs x %d gradient buffers) exceeds the handle's "
+                "arena of %lld bytes (raise zero_opt_config.table_kib)",
+                (long long)blob.size(), nseg, nbuf, (long long)h->table_bytes);
+  if ((int)h->plans.size() >= kMaxPlans) {
+    auto lru = h->plans.end();
+    for (auto it = h->plans.begin(); it != h->plans.end(); ++it)
+      if (!(*it)->pinned && (lru == h->plans.end() || (*it)->stamp < (*lru)->stamp)) lru = it;
+    if (lru == h->plans.end())
+      return fail(ZERO_ERANGE, "all %d run tables are pinned by stream captures", kMaxPlans);
+    zero_status st = evict(h, lru);
+    if (st != ZERO_OK) return st;
   }
+  int64_t off = 0;
+  zero_status st = place(h, size, &off);
+  if (st != ZERO_OK) return st;
   Plan* p = new Plan;
   p->blob = std::move(blob);
+  p->hash = hash;
+  p->off = off;
+  p->size = size;
   p->nseg = nseg;
   p->nbuf = nbuf;
   p->ntiles = tile0;
   p->stamp = h->clock;
-  if (!p->blob.empty()) {
-    cudaError_t e = cudaMalloc(&p->dev, p->blob.size());
-    if (e != cudaSuccess) {
-      delete p;
-      return cuda_fail(e, "cudaMalloc(plan)");
-    }
-    // From pageable memory: staged before the call returns, and ordered on
-    // `stream` before the kernels that read the table.
-    e = cudaMemcpyAsync(p->dev, p->blob.data(), p->blob.size(), cudaMemcpyHostToDevice, stream);
-    if (e != cudaSuccess) {
-      cudaFree(p->dev);
-      delete p;
-      return cuda_fail(e, "cudaMemcpyAsync(plan)");
-    }
+  p->ev = h->free_ev.back();
+  h->free_ev.pop_back();
+  // The pinned mirror is not touched again until this copy has run (its event
+  // is waited on before the bytes are reused).
+  std::memcpy(h->table_host + off, p->blob.data(), p->blob.size());
+  e = cudaMemcpyAsync(h->table_dev + off, h->table_host + off, p->blob.size(),
+                      cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess) e = cudaEventRecord(h->table_ev[p->ev], stream);
+  if (e != cudaSuccess) {
+    h->free_ev.push_back(p->ev);
+    delete p;
+    return cuda_fail(e, "run-table upload");
   }
+  h->table_uploads += 1;
   h->plans.push_back(p);
   *out = p;
   return ZERO_OK;
@@ -411,9 +557,11 @@ zero_status run(zero_opt_t h, int32_t rank, const std::vector<HostRun>& runs, in
   zero_status st = get_plan(h, runs, nbuf, use_stash, stream, &plan);
   if (st != ZERO_OK) return st;
 
-  const zo::Seg* segs = static_cast<const zo::Seg*>(plan->dev);
-  const void* const* gptrs = reinterpret_cast<const void* const*>(
-      static_cast<const unsigned char*>(plan->dev) + sizeof(zo::Seg) * plan->nseg);
+  const unsigned char* table = plan->off >= 0 ? h->table_dev + plan->off : nullptr;
+  const zo::Seg* segs = reinterpret_cast<const zo::Seg*>(table);
+  const void* const* gptrs =
+      table ? reinterpret_cast<const void* const*>(table + sizeof(zo::Seg) * plan->nseg)
+            : nullptr;
 
   zo::Pass1Args a1;
   std::memset(&a1, 0, sizeof(a1));
@@ -647,7 +795,7 @@ zero_status zero_opt_create(const zero_opt_config* cfg, zero_opt_t* out) {
     e = cudaDeviceGetAttribute(&h->sms, cudaDevAttrMultiProcessorCount, h->device);
   const size_t ws_bytes = sizeof(zo::Workspace) + sizeof(zo::RankState) * (size_t)cfg->world;
   void* ws = nullptr;
-  if (e == cudaSuccess) e = cudaMalloc(&ws, ws_bytes);
+  if (e == cudaSuccess) e = handle_malloc(h, &ws, ws_bytes);
   if (e != cudaSuccess) {
     delete h;
     return e == cudaErrorMemoryAllocation ? fail(ZERO_ENOMEM, "workspace allocation failed")
@@ -669,8 +817,21 @@ zero_status zero_opt_create(const zero_opt_config* cfg, zero_opt_t* out) {
     r0[r].reserved = 0;
   }
   e = cudaMemcpy(ws, init.data(), ws_bytes, cudaMemcpyHostToDevice);
-  if (e == cudaSuccess) e = cudaMallocHost(&h->pinned, kPinnedBytes);
-  if (e == cudaSuccess) e = cudaMalloc(&h->bc_table, sizeof(double) * 2 * zo::kBcSteps);
+  if (e == cudaSuccess) e = handle_malloc_host(h, &h->pinned, kPinnedBytes);
+  if (e == cudaSuccess)
+    e = handle_malloc(h, reinterpret_cast<void**>(&h->bc_table),
+                      sizeof(double) * 2 * zo::kBcSteps);
+  // the run-table arena and its page-locked mirror: every table a step needs
+  // is placed here, so no step allocates
+  h->table_bytes = cfg->table_kib > 0 ? (int64_t)cfg->table_kib * 1024 : kDefaultTableBytes;
+  if (e == cudaSuccess)
+    e = handle_malloc(h, reinterpret_cast<void**>(&h->table_dev), (size_t)h->table_bytes);
+  if (e == cudaSuccess)
+    e = handle_malloc_host(h, reinterpret_cast<void**>(&h->table_host), (size_t)h->table_bytes);
+  for (int i = 0; i < kMaxPlans && e == cudaSuccess; ++i) {
+    e = cudaEventCreateWithFlags(&h->table_ev[i], cudaEventDisableTiming);
+    if (e == cudaSuccess) h->free_ev.push_back(kMaxPlans - 1 - i);
+  }
   if (e == cudaSuccess) {
     zo::BcTableArgs ta;
     ta.table = h->bc_table;
@@ -684,13 +845,19 @@ zero_status zero_opt_create(const zero_opt_config* cfg, zero_opt_t* out) {
     if (e == cudaSuccess) e = cudaStreamSynchronize(nullptr);
   }
   if (e != cudaSuccess) {
-    cudaFree(h->bc_table);
-    if (h->pinned) cudaFreeHost(h->pinned);
-    cudaFree(ws);
+    for (cudaEvent_t ev : h->table_ev)
+      if (ev) cudaEventDestroy(ev);
+    handle_free(h, h->table_dev);
+    handle_free_host(h, h->table_host);
+    handle_free(h, h->bc_table);
+    handle_free_host(h, h->pinned);
+    handle_free(h, ws);
     delete h;
-    return cuda_fail(e, "zero_opt_create");
+    return e == cudaErrorMemoryAllocation ? fail(ZERO_ENOMEM, "zero_opt_create: out of memory")
+                                          : cuda_fail(e, "zero_opt_create");
   }
   h->has_device = true;
+  h->created = true;
   *out = h;
   return ZERO_OK;
 }
@@ -702,13 +869,15 @@ zero_status zero_opt_destroy(zero_opt_t h) {
     cudaGetDevice(&prev);
     cudaSetDevice(h->device);
     cudaDeviceSynchronize();
-    for (Plan* p : h->plans) {
-      if (p->dev) cudaFree(p->dev);
-      delete p;
-    }
-    cudaFree(h->ws);
-    cudaFree(h->bc_table);
-    cudaFreeHost(h->pinned);
+    h->created = false;  // the frees of destruction are not counted
+    for (Plan* p : h->plans) delete p;
+    for (cudaEvent_t ev : h->table_ev)
+      if (ev) cudaEventDestroy(ev);
+    handle_free(h, h->table_dev);
+    handle_free_host(h, h->table_host);
+    handle_free(h, h->ws);
+    handle_free(h, h->bc_table);
+    handle_free_host(h, h->pinned);
     if (prev >= 0) cudaSetDevice(prev);
   }
   delete h;
@@ -1074,6 +1243,22 @@ zero_status zero_opt_inject_wait_fault(zero_opt_t h) {
 zero_status zero_opt_launch_count(zero_opt_t h, int64_t* launches) {
   if (!h || !launches) return fail(ZERO_EINVAL, "NULL argument");
   *launches = h->launches;
+  return ZERO_OK;
+}
+
+zero_status zero_opt_get_counters(zero_opt_t h, zero_opt_counters* out) {
+  if (!h || !out) return fail(ZERO_EINVAL, "NULL argument");
+  std::lock_guard<std::mutex> lock(h->mu);
+  out->launches = h->launches;
+  out->table_uploads = h->table_uploads;
+  out->table_waits = h->table_waits;
+  out->device_allocs = h->device_allocs;
+  out->device_frees = h->device_frees;
+  out->tables_cached = (int64_t)h->plans.size();
+  int64_t pinned = 0;
+  for (const Plan* p : h->plans) pinned += p->pinned ? 1 : 0;
+  out->tables_pinned = pinned;
+  out->table_bytes = h->table_bytes;
   return ZERO_OK;
 }
 
