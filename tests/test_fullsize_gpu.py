@@ -4,13 +4,21 @@ configuration bench.py times, checked on sampled outputs.
 The oracle computes each step's global statistics exactly over the whole
 gradient buffers (copied to the host in chunks), takes its own decisions and
 updates the sampled elements one by one; the GPU's outputs at those indices
-must match (fp32 state 1e-6 relative, abs 1e-9; 16-bit copy 1 ulp; norm 1e-5;
-skip and scale bit-exact).  An overflow is injected on the second step.
+must match after every step (fp32 state 1e-6 relative, abs 1e-9; 16-bit copy
+1 ulp; norm 1e-5; skip and scale bit-exact).
+
+The GPT-2-sized buffer runs its 100 steps with the clip active, and the
+Llama-3-8B ZeRO-2 shard its 100 steps under a dynamic scale of 2^16 with an
+overflow injected every 50 steps at a seeded index: those two steps are
+skipped and halve the scale, which ends at 2^14 ("DeepSpeed tutorial" §2.2,
+§3.2: skip and lower the scale on overflow; window 1000, so no growth).  The
+other workloads run three steps with an overflow on the second.
 """
 import numpy as np
 import pytest
 
 import oracle as O
+import synth
 from harness import assert_state, to_np16, ulp16_diff
 
 pytestmark = pytest.mark.gpu
@@ -120,31 +128,48 @@ class Run:
             assert ulp16_diff(to_np16(p16[ti]), smp["p16"]) <= 1
 
 
-def _run(name, steps=3, inject_step=2):
+def _run(name, steps=3, inject_steps=(2,)):
+    """`steps` steps of workload `name`; on each step of `inject_steps` a +inf
+    replaces one gradient at an index drawn from the seeded generator."""
     import zero_sharded_mixed_05_gb300 as z
     run = Run(name)
+    n0 = run.groups[0][1].numel()
+    where = synth.seeded_indices(run.s.w["seed"], 99, len(inject_steps), 0, n0)
+    inject_at = dict(zip(inject_steps, where))
+    skipped, norms = [], []
     try:
         for step in range(1, steps + 1):
-            inject = (0, 12_345) if step == inject_step else None
+            inject = (0, inject_at[step]) if step in inject_at else None
             info, d, G = run.step(inject)
-            assert info.skipped == d.skip == (1 if step == inject_step else 0)
+            assert info.skipped == d.skip == (1 if step in inject_at else 0)
             assert info.scale_used == d.scale_used
             assert info.t == run.sc.t
             if not d.skip:
                 assert abs(info.norm - d.norm) <= 1e-5 * d.norm
                 assert abs(info.sumsq - G.sumsq) <= 1e-5 * G.sumsq
+                norms.append(d.norm)
+            else:
+                skipped.append(step)
             assert z.zero_opt_loss_scale(run.s.h, 0).as_tuple() == run.sc.as_tuple()
             run.check()
+        return run.sc.as_tuple(), skipped, norms
     finally:
         z.zero_opt_destroy(run.s.h)
 
 
-def test_fullsize_gpt2():
-    _run("gpt2")
+def test_fullsize_gpt2_100_steps():
+    """GPT-2 size, 100 steps, no loss scaling, the clip active throughout."""
+    (scale, clean, t, skipped_total, last), skipped, norms = _run("gpt2", 100, ())
+    assert (scale, t, skipped_total, skipped) == (1.0, 100, 0, [])
+    assert min(norms) > 1.0          # above max_grad_norm: every step is clipped
 
 
-def test_fullsize_llama_zero2_shard():
-    _run("llama")
+def test_fullsize_llama_zero2_shard_100_steps():
+    """The 1,003,782,656-parameter ZeRO-2 shard for 100 steps with overflows
+    on steps 50 and 100: both skipped, the scale 2^16 -> 2^15 -> 2^14."""
+    (scale, clean, t, skipped_total, last), skipped, _ = _run("llama", 100, (50, 100))
+    assert skipped == [50, 100]
+    assert (scale, t, skipped_total, last) == (2.0 ** 14, 98, 2, 1)
 
 
 def test_fullsize_fused_reduce():
