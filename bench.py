@@ -17,10 +17,14 @@ clip, AdamW, 16-bit copy).
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload pertensor|gpt2|gpt2_master16|llama|fused]
 
-Prints one JSON line (rank 0).  Under torchrun every rank runs its own copy of
-the workload on its own GPU (weak scaling) and the timing is the maximum over
-ranks.  --impl reference times the CPU oracle (single-threaded C++) on a
-bounded sample of the same workload.
+Prints one JSON line (rank 0).  Under torchrun with N > 1 ranks it times the
+sharded ZeRO-2 step of the same model over the N GPUs (strong scaling: each
+rank owns 1/N of the parameters; all-to-all of the gradient bytes, statistics
+folded on the device, all-gather of the 16-bit parameters; --zero3 keeps them
+sharded), the timing being the maximum over ranks; --replicas instead runs an
+independent copy of the one-GPU workload per rank (weak scaling).  --zero2 /
+--zero3 select the sharded step on one GPU too.  --impl reference times the
+CPU oracle (single-threaded C++) on a bounded sample of the same workload.
 """
 from __future__ import annotations
 
@@ -671,13 +675,17 @@ def run_ours(args):
     return 0
 
 
-def run_zero2(args):
-    """The ZeRO-2 data-parallel step over the process group (Zero2Step with
-    the device kernels, NCCL): each rank holds its local gradients for the
-    whole model (N shards of the workload's size, K micro-steps), sends every
-    shard's bytes to its owner (all-to-all), steps its own shard and
-    all-gathers the 16-bit parameters.  Opt-in (--zero2); prints its own JSON
-    line with the whole model's params/s."""
+def run_sharded(args, stage):
+    """The ZeRO-2 (stage 2) or ZeRO-3 (stage 3) data-parallel step of the
+    workload's whole model sharded over the process group's N ranks (strong
+    scaling: the model is fixed, each rank owns S = ceil(Psi / N) parameters).
+    Every rank holds its local gradients for the whole model (K buffers of P
+    elements), sends each shard's bytes to its owner (all-to-all), the owner
+    folds the N ranks' statistics on the device and steps its shard, and under
+    ZeRO-2 the 16-bit parameters are all-gathered.  The per-tensor list is
+    taken as its flat concatenation (2,270,232,576 parameters), as a ZeRO
+    engine keeps its gradients in contiguous buffers.  Prints one JSON line
+    with the whole model's params/s."""
     import torch
     import torch.distributed as dist
 
@@ -687,16 +695,17 @@ def run_zero2(args):
     dev = torch.device("cuda", local)
     os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
     os.environ.setdefault("MASTER_PORT", "29511")
+    os.environ.setdefault("NCCL_NVLS_ENABLE", "0")
     dist.init_process_group("nccl", rank=rank, world_size=ws, device_id=dev)
     import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    dist.barrier()
     __graft_entry__.build()
     import zero_sharded_mixed_05_gb300 as z
-    from zero_sharded_mixed_05_gb300.distributed import Zero2Step
+    from zero_sharded_mixed_05_gb300.distributed import ZeroStep
     w = WORKLOADS[args.workload]
-    if args.workload == "pertensor":
-        raise SystemExit("--zero2 applies to flat workloads")
-    S, K = w["numel"], w["K"]
-    psi = S * ws
+    psi, K = w["numel"], w["K"]           # the process group's ranks replace R
     code = z.FP16 if w["dtype"] == "fp16" else z.BF16
     kind = synth.F16 if code == z.FP16 else synth.BF16
     tdt = torch.float16 if code == z.FP16 else torch.bfloat16
@@ -704,43 +713,118 @@ def run_zero2(args):
                         max_grad_norm=w["clip"], dynamic_scale=w["dynamic"],
                         init_scale=w["scale"], scale_window=1000,
                         master16=w.get("master16", False))
-    zs = Zero2Step(cfg, backend="device")
-    master = torch.empty(S, dtype=torch.float32, device=dev)
-    synth.fill_gpu(master, w["seed"], 0, rank * S, 0.02, synth.F32)
+    zs = ZeroStep(cfg, backend="device", stage=stage)
+    S, P = zs.S, zs.P
+    b0, e0 = rank * S, min(psi, (rank + 1) * S)
+    master = torch.zeros(S, dtype=torch.float32, device=dev)
+    if e0 > b0:
+        synth.fill_gpu(master[:e0 - b0], w["seed"], 0, b0, 0.02, synth.F32)
     m, v = torch.zeros(S, device=dev), torch.zeros(S, device=dev)
-    p16 = torch.zeros(psi, dtype=tdt, device=dev)
-    p16[rank * S:(rank + 1) * S].copy_(master)
+    if stage == 2:
+        p16 = torch.zeros(P, dtype=tdt, device=dev)
+        p16[b0:b0 + S].copy_(master)
+        own16 = p16[b0:b0 + S]
+    else:
+        p16 = master.to(tdt)
+        own16 = p16
     if w.get("master16"):
         master = None
     grads = []
     for k in range(K):
-        g = torch.empty(psi, dtype=tdt, device=dev)
-        synth.fill_gpu(g, w["seed"], 1 + rank * K + k, 0, w["sigma"] * w["scale"], kind)
+        g = torch.zeros(P, dtype=tdt, device=dev)
+        synth.fill_gpu(g[:psi], w["seed"], 1 + rank * K + k, 0, w["sigma"] * w["scale"], kind)
         grads.append(g)
+    stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
         zs.step(grads, master, m, v, p16)
-    dist.barrier()
     torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
-    for _ in range(args.steps):
+    dist.barrier()
+    EVERY = 8
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
+           for _ in range(0, args.steps, EVERY)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    t_spin = time.time()
+    while time.time() - t_spin < 0.3:
         zs.step(grads, master, m, v, p16)
-    b.record()
+    launches0 = z.zero_opt_launch_count(zs.h)
     torch.cuda.synchronize()
     dist.barrier()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    a.record(stream)
+    for i in range(args.steps):
+        if i % EVERY == 0:
+            z.zero_opt_set_events(zs.h, *evs[i // EVERY])
+            zs.step(grads, master, m, v, p16)
+            z.zero_opt_set_events(zs.h)
+        else:
+            zs.step(grads, master, m, v, p16)
+    b.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    launches = z.zero_opt_launch_count(zs.h) - launches0
+    dist.barrier()
+    clocks.stop()
+    clk = clocks.summary(t0, t1)
     ms = max_over_ranks(a.elapsed_time(b) / args.steps, dev)
+    p2_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    p2_ms = max_over_ranks(p2_ms, dev)
+    nbuf = ws * K
+    p2_bytes = (2 * nbuf + state_bytes_per_param(w)) * S
+    peak, peak_src = load_peaks()
+    # end to end: each step's local gradients come up from pinned host memory
+    # and the rank's updated 16-bit shard goes back down, on the step's stream
+    host_g = [torch.empty(g.shape, dtype=g.dtype, pin_memory=True) for g in grads]
+    for hg, g in zip(host_g, grads):
+        hg.copy_(g)
+    host_p = torch.empty(own16.shape, dtype=own16.dtype, pin_memory=True)
+    ke = max(3, min(args.steps, 20))
+    torch.cuda.synchronize()
+    dist.barrier()
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ea.record(stream)
+    for _ in range(ke):
+        for hg, g in zip(host_g, grads):
+            g.copy_(hg, non_blocking=True)
+        zs.step(grads, master, m, v, p16)
+        host_p.copy_(own16, non_blocking=True)
+    eb.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(ea.elapsed_time(eb) / ke, dev)
     if rank == 0:
+        name = "ZeRO-2" if stage == 2 else "ZeRO-3"
         print(json.dumps({
-            "metric": METRIC, "value": psi / (ms * 1e-3), "unit": "params/s", "impl": "zero2",
-            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "metric": METRIC, "value": psi / (ms * 1e-3), "unit": "params/s",
+            "impl": "zero%d" % stage, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "scaling": "strong",
+            "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded SplitMix64 / Irwin-Hall), resident in HBM",
-            "config": {"workload": w["desc"] + " [ZeRO-2 across the ranks: all-to-all of the "
-                       "gradient bytes, step of the own shard, all-gather of the 16-bit "
-                       "parameters]", "params_per_gpu": S, "params_total": psi,
-                       "micro_steps": K, "parallelism": f"zero2-dp{ws}"}}))
+            "config": {"workload": w["desc"] + f" [{name} across the {ws} ranks: all-to-all of "
+                       "the gradient bytes, statistics folded on the device, step of the own "
+                       "shard" + (", all-gather of the 16-bit parameters" if stage == 2 else
+                                  "; 16-bit parameters stay sharded") + "]",
+                       "params_total": psi, "params_per_gpu": S, "micro_steps": K,
+                       "parallelism": f"zero{stage}-dp{ws}",
+                       "l2": "inputs larger than L2"},
+            "roofline": {"bound": "hbm", "kernel": "pass2_kernel (unscale+clip+AdamW+cast) "
+                         f"over the {nbuf} received shard buffers",
+                         "achieved": p2_bytes / (p2_ms * 1e-3) / 1e9, "peak": peak,
+                         "unit": "GB/s", "frac": p2_bytes / (p2_ms * 1e-3) / 1e9 / peak,
+                         "peak_source": peak_src + " (hbm_gbs)", "traffic": None,
+                         "bytes_per_launch": p2_bytes, "avg_launch_ms": p2_ms,
+                         "timing": "CUDA events around each pass on every %d-th timed "
+                                   "step" % EVERY},
+            "e2e": {"value": psi / (e2e_ms * 1e-3), "unit": "params/s",
+                    "h2d_bytes_per_step": sum(g.numel() * 2 for g in grads),
+                    "d2h_bytes_per_step": own16.numel() * 2, "ms_per_step": e2e_ms,
+                    "transfers": "pinned host buffers, copies in line with the step on its "
+                                 "stream (each rank's local gradients up, its 16-bit shard "
+                                 "down)"},
+            "gpu_launches": launches, "clocks": clk}))
     zs.close()
     dist.destroy_process_group()
+    return 0
 
 
 def run_offload(args):
@@ -810,7 +894,13 @@ def main():
     ap.add_argument("--no-e2e", action="store_true",
                     help="leave out the end-to-end and copy-ceiling legs (profiling runs)")
     ap.add_argument("--zero2", action="store_true",
-                    help="time the ZeRO-2 step with its collectives over the process group")
+                    help="time the sharded ZeRO-2 step with its collectives over the process "
+                         "group (the default under torchrun with more than one rank)")
+    ap.add_argument("--zero3", action="store_true",
+                    help="time the sharded ZeRO-3 step (16-bit parameters stay sharded)")
+    ap.add_argument("--replicas", action="store_true",
+                    help="under torchrun, time independent replicas of the one-GPU step "
+                         "instead of the sharded step")
     ap.add_argument("--offload", action="store_true",
                     help="time the offloaded step (CPU threads, host buffers) instead")
     ap.add_argument("--threads", type=int, default=0,
@@ -837,8 +927,11 @@ def main():
         return run_reference(args)
     if args.offload:
         return run_offload(args)
-    if args.zero2:
-        return run_zero2(args)
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.zero3:
+        return run_sharded(args, 3)
+    if args.zero2 or (ws > 1 and not args.replicas):
+        return run_sharded(args, 2)
     return run_ours(args)
 
 

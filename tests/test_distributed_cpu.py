@@ -1,10 +1,12 @@
-"""The ZeRO-2 step across two processes (gloo, CPU, the host back end):
-all-to-all of the raw 16-bit gradient slices, local binary32 reduction in rank
-order, the two-scalar fold, the shard step and the all-gather of the 16-bit
-parameters.  Every rank's shard state and the gathered parameter buffer must be
-bit-identical to the oracle's one-process step over the same gradients (each
-rank's K micro-step buffers, rank-major), including a step whose overflow sits
-on the other rank's gradient.  No GPU is touched."""
+"""The ZeRO-2 and ZeRO-3 steps across two processes (gloo, CPU, the host back
+end): all-to-all of the raw 16-bit gradient slices, local binary32 reduction in
+rank order, the two-scalar fold, the shard step and, under ZeRO-2, the
+all-gather of the 16-bit parameters (under ZeRO-3 each rank keeps only its
+parameter shard; the full buffer is gathered on request).  Every rank's shard
+state and parameters must be bit-identical to the oracle's one-process step
+over the same gradients (each rank's K micro-step buffers, rank-major),
+including a step whose overflow sits on the other rank's gradient.  No GPU is
+touched."""
 import os
 import socket
 
@@ -46,7 +48,7 @@ def _cfg_kwargs(master16):
                 dynamic_scale=True, init_scale=64.0, scale_window=1000, master16=master16)
 
 
-def _worker(rank, port, out_dir, code, master16):
+def _worker(rank, port, out_dir, code, master16, stage=2):
     import sys
     sys.path.insert(0, ROOT)
     import torch
@@ -55,12 +57,12 @@ def _worker(rank, port, out_dir, code, master16):
     import oracle as O
     import synth
     import zero_sharded_mixed_05_gb300 as z
-    from zero_sharded_mixed_05_gb300.distributed import Zero2Step
+    from zero_sharded_mixed_05_gb300.distributed import Zero2Step, Zero3Step
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
     dist.init_process_group("gloo", rank=rank, world_size=WORLD)
     cfg = z.make_config(grad_dtype=code, **_cfg_kwargs(master16))
-    zs = Zero2Step(cfg, backend="host", threads=2)
+    zs = (Zero2Step if stage == 2 else Zero3Step)(cfg, backend="host", threads=2)
     b, e, S, P = O.shard_bounds(NUMEL, WORLD, rank)
     p0 = synth.normal_np(SEED, 0, 0, NUMEL, 0.02, synth.F32)
     tdt = torch.float16 if code == 0 else torch.bfloat16
@@ -71,6 +73,8 @@ def _worker(rank, port, out_dir, code, master16):
     p16 = torch.zeros(P, dtype=torch.int16)
     p16[:NUMEL] = torch.from_numpy(q0.view(np.int16)) if master16 else 0
     p16 = p16.view(tdt)
+    if stage == 3:
+        p16 = p16[b:b + S].clone()          # ZeRO-3: this rank's shard only
     scale = 64.0
     infos = []
     for step in range(1, STEPS + 1):
@@ -80,21 +84,26 @@ def _worker(rank, port, out_dir, code, master16):
         info = zs.last_step()
         infos.append((info.skipped, info.scale_used, info.t, info.coef))
         scale = z.zero_host_loss_scale(zs.h, rank).scale
+    shard16 = p16.view(torch.int16).numpy().view(np.uint16).copy()
+    if stage == 3:
+        p16 = zs.gather_params(p16)          # the full buffer, for a forward pass
     np.savez(os.path.join(out_dir, f"r{rank}.npz"), master=master.numpy(), m=m.numpy(),
              v=v.numpy(), p16=p16.view(torch.int16).numpy().view(np.uint16),
-             infos=np.array(infos, dtype=np.float64))
+             shard16=shard16, infos=np.array(infos, dtype=np.float64))
     zs.close()
     dist.barrier()
     dist.destroy_process_group()
 
 
-@pytest.mark.parametrize("code,master16", [(0, False), (1, True)], ids=["fp16", "bf16-master16"])
-def test_two_rank_zero2_step_matches_the_oracle(tmp_path, code, master16):
+@pytest.mark.parametrize("code,master16,stage",
+                         [(0, False, 2), (1, True, 2), (0, False, 3), (1, True, 3)],
+                         ids=["fp16", "bf16-master16", "zero3-fp16", "zero3-bf16-master16"])
+def test_two_rank_zero_step_matches_the_oracle(tmp_path, code, master16, stage):
     from zero_sharded_mixed_05_gb300 import _build
     _build.build()
     import oracle as O
     import synth
-    spawn_bounded(_worker, (_free_port(), str(tmp_path), code, master16), WORLD)
+    spawn_bounded(_worker, (_free_port(), str(tmp_path), code, master16, stage), WORLD)
     res = [np.load(os.path.join(tmp_path, f"r{r}.npz")) for r in range(WORLD)]
     # the oracle: the one-process step of every shard with R = WORLD ranks' K buffers each
     orc = O.default()
@@ -130,7 +139,9 @@ def test_two_rank_zero2_step_matches_the_oracle(tmp_path, code, master16):
             assert (got["master"][:e - b].view(np.uint32) == st[r][0].view(np.uint32)).all()
         assert (got["m"][:e - b].view(np.uint32) == st[r][1].view(np.uint32)).all()
         assert (got["v"][:e - b].view(np.uint32) == st[r][2].view(np.uint32)).all()
-        # the gathered parameter buffer on every rank holds every shard
+        # the rank's own 16-bit shard (the ZeRO-3 step's whole output), and
+        # the gathered buffer (ZeRO-2 after every step; ZeRO-3 on request)
+        assert (got["shard16"][b - (b if stage == 3 else 0):][:e - b] == st[r][3]).all()
         for j, (bj, ej, _, _) in enumerate(bounds):
             assert (got["p16"][bj:ej] == st[j][3]).all(), (r, j)
         assert not got["p16"][NUMEL:].any()

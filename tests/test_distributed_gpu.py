@@ -1,8 +1,8 @@
-"""The ZeRO-2 step's device back end (CUDA kernels, NCCL process group) in
-one process on one GPU.  With one rank the exchanges are copies, so this
-checks the device path's plumbing: byte-view collectives on device tensors,
-stream order between the collectives and the kernels, the fold and the
-in-place gather.  The state must match the oracle's one-process step bit for
+"""The ZeRO-2 and ZeRO-3 steps' device back end (CUDA kernels, NCCL process
+group) in one process on one GPU.  With one rank the exchanges are copies, so
+this checks the device path's plumbing: byte-view collectives on device
+tensors, stream order between the collectives and the kernels, the fold, the
+in-place gather (ZeRO-2) and the shard-local 16-bit parameters (ZeRO-3).  The state must match the oracle's one-process step bit for
 bit (no clipping, so the coefficient does not depend on the norm's last
 bits).  The exchange logic across ranks is covered on the CPU by
 test_distributed_cpu.py."""
@@ -40,7 +40,7 @@ def _grads(step, scale):
     return out
 
 
-def _worker(rank, port, out_path):
+def _worker(rank, port, out_path, stage=2):
     import sys
     sys.path.insert(0, ROOT)
     import torch
@@ -48,7 +48,7 @@ def _worker(rank, port, out_path):
 
     import synth
     import zero_sharded_mixed_05_gb300 as z
-    from zero_sharded_mixed_05_gb300.distributed import Zero2Step
+    from zero_sharded_mixed_05_gb300.distributed import ZeroStep
     os.environ["MASTER_ADDR"] = "127.0.0.1"
     os.environ["MASTER_PORT"] = str(port)
     os.environ.setdefault("NCCL_NVLS_ENABLE", "0")
@@ -56,7 +56,7 @@ def _worker(rank, port, out_path):
     dist.init_process_group("nccl", rank=0, world_size=1, device_id=torch.device("cuda", 0))
     cfg = z.make_config(numel=NUMEL, world=1, grad_dtype=z.FP16, lr=1e-3, weight_decay=0.01,
                         dynamic_scale=True, init_scale=128.0)
-    zs = Zero2Step(cfg, backend="device")
+    zs = ZeroStep(cfg, backend="device", stage=stage)
     dev = torch.device("cuda", 0)
     master = torch.from_numpy(synth.normal_np(SEED, 0, 0, NUMEL, 0.02, synth.F32)).to(dev)
     m, v = torch.zeros(NUMEL, device=dev), torch.zeros(NUMEL, device=dev)
@@ -76,7 +76,8 @@ def _worker(rank, port, out_path):
     dist.destroy_process_group()
 
 
-def test_one_rank_device_zero2_step(tmp_path):
+@pytest.mark.parametrize("stage", [2, 3])
+def test_one_rank_device_zero_step(tmp_path, stage):
     import torch
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA device")
@@ -85,7 +86,7 @@ def test_one_rank_device_zero2_step(tmp_path):
     import oracle as O
     import synth
     out = os.path.join(tmp_path, "r0.npz")
-    spawn_bounded(_worker, (_free_port(), out), 1)
+    spawn_bounded(_worker, (_free_port(), out, stage), 1)
     got = np.load(out)
     orc = O.default()
     hp = O.hparams(lr=1e-3, weight_decay=0.01, dynamic_scale=True, scale_window=1000)
