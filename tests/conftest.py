@@ -37,7 +37,10 @@ def read_golden(name):
 
 def spawn_bounded(fn, args, nprocs, seconds=300):
     """torch.multiprocessing.spawn with a time limit: children still running
-    after `seconds` are terminated and the test fails instead of waiting."""
+    after `seconds` are terminated (SIGTERM), and any that are still alive
+    after a short grace period -- e.g. blocked inside a CUDA or NCCL call that
+    does not return to the interpreter -- are killed (SIGKILL); the test then
+    fails instead of waiting."""
     import time
 
     import torch.multiprocessing as tmp
@@ -48,4 +51,10 @@ def spawn_bounded(fn, args, nprocs, seconds=300):
             for p in ctx.processes:
                 if p.is_alive():
                     p.terminate()
+            for p in ctx.processes:
+                p.join(timeout=10)
+            for p in ctx.processes:
+                if p.is_alive():
+                    p.kill()
+                    p.join(timeout=10)
             raise AssertionError(f"spawned ranks did not finish within {seconds} s")

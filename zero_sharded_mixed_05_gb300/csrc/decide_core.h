@@ -4,12 +4,17 @@
 // host (offloaded) step, so both take the same decisions from the same
 // statistics.  Plain C++ apart from the host/device qualifiers.
 //
-// Sources ("DeepSpeed tutorial", §3 mixed precision and §3 optimizer config;
-// "ZeRO paper notes", Adam update): a step whose reduced gradients hold an inf
-// or NaN is skipped and lowers the loss scale (not below min_loss_scale); the
-// scale grows by the factor after loss_scale_window consecutive applied steps;
-// Adam keeps first and second moments with bias correction, eps outside the
-// root, and AdamW's weight decay is decoupled.  Readings where the pages are
+// Sources: "DeepSpeed tutorial" (devpress.csdn.net) §2.2 (loss scaling: a
+// step whose gradients overflow is skipped and lowers the scale, which rises
+// again once training is stable) and §3.2 (the ds_config.json fp16 block:
+// loss_scale 0 for dynamic scaling, initial_scale_power, loss_scale_window,
+// hysteresis, min_loss_scale; the AdamW optimizer block and the WarmupLR
+// scheduler block); "DeepSpeed ZeRO引擎深入" (aiqz.cc), "Python 演示" (the Adam
+// update: first and second moments, eps added outside the square root).  So:
+// an inf or NaN in the reduced gradients skips the step and lowers the loss
+// scale (not below min_loss_scale); the scale grows by the factor after
+// loss_scale_window consecutive applied steps; Adam keeps m and v with bias
+// correction, eps outside the root, and AdamW's weight decay is decoupled.  Readings where the pages are
 // silent: the global L2 norm of the unscaled gradient with coefficient
 // min(1, max_norm / (norm + 1e-6)); hysteresis lowers the scale on the
 // hysteresis-th overflow since it last changed; WarmupLR ramps the lr linearly
