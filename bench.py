@@ -98,11 +98,13 @@ WORKLOADS = {
 
 
 # Committed ncu summaries of one pass-2 launch per workload, from which the
-# per-parameter DRAM traffic is read (scaled to the workload by its parameter
-# count: the kernel streams, so its traffic is proportional to the elements).
+# per-parameter DRAM traffic is read (times the workload's parameter count;
+# the per-tensor list's was captured at its full size, GPT-2's at 100M
+# parameters: the kernel streams, so its traffic is proportional to the
+# elements).
 PASS2_PROFILES = {
     "gpt2": "pass2_kernel_gpt2_100M_ncu_full.md",
-    "pertensor": "pass2_kernel_pertensor_div4_ncu_full.md",
+    "pertensor": "pass2_kernel_pertensor_full_dram.md",
 }
 
 
@@ -312,6 +314,19 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- arms
 
+def emit(line):
+    """Print the bench's JSON line as the last line of stdout: anything a
+    native library (NCCL's version banner) left in the C stdio buffer is
+    flushed first."""
+    import ctypes
+    sys.stdout.flush()
+    try:
+        ctypes.CDLL(None).fflush(None)
+    except (OSError, AttributeError):
+        pass
+    print(json.dumps(line), flush=True)
+
+
 def max_over_ranks(value: float, device) -> float:
     """Largest value over the ranks of the default process group."""
     import torch
@@ -397,7 +412,7 @@ def run_reference(args):
             "cpu_baseline": {"value": value, "unit": "params/s", **sample.info()},
             "e2e": {"value": value, "unit": "params/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
-    print(json.dumps(line))
+    emit(line)
     return 0
 
 
@@ -632,7 +647,7 @@ def run_ours(args):
         tpp = None                    # a resized workload has no committed capture
     traffic = tpp * n if tpp is not None else None
     traffic_src = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one pass-2 launch, "
-                   "per parameter, scaled to this workload by parameter count (%s)" % tsrc
+                   "per parameter, times this workload's parameters (%s)" % tsrc
                    if traffic is not None else None)
 
     cpu = None
@@ -669,9 +684,10 @@ def run_ours(args):
         }
         if cpu is not None:
             line["cpu_baseline"] = cpu
-        print(json.dumps(line))
     if ws > 1:
         torch.distributed.destroy_process_group()
+    if rank == 0:
+        emit(line)
     return 0
 
 
@@ -742,6 +758,9 @@ def run_sharded(args, stage):
     EVERY = 8
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)]
            for _ in range(0, args.steps, EVERY)]
+    for trio in evs:
+        for e in trio:
+            e.record(stream)   # torch times only events it has recorded once
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     t_spin = time.time()
@@ -792,9 +811,10 @@ def run_sharded(args, stage):
     eb.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(ea.elapsed_time(eb) / ke, dev)
+    line = None
     if rank == 0:
         name = "ZeRO-2" if stage == 2 else "ZeRO-3"
-        print(json.dumps({
+        line = {
             "metric": METRIC, "value": psi / (ms * 1e-3), "unit": "params/s",
             "impl": "zero%d" % stage, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "scaling": "strong",
@@ -821,9 +841,11 @@ def run_sharded(args, stage):
                     "transfers": "pinned host buffers, copies in line with the step on its "
                                  "stream (each rank's local gradients up, its 16-bit shard "
                                  "down)"},
-            "gpu_launches": launches, "clocks": clk}))
+            "gpu_launches": launches, "clocks": clk}
     zs.close()
     dist.destroy_process_group()
+    if line is not None:
+        emit(line)
     return 0
 
 
