@@ -507,19 +507,37 @@ __device__ __forceinline__ double block_sum(double x, double* red) {
 // Run by thread 0 of pass 1's scalar CTA while the other CTAs stream: the
 // scalars of the step that follows the current one (t + 1; the step counter
 // only changes in the decision at the end of this launch), so that the
-// decision, which waits for every CTA, does no binary64 pow.
+// decision, which waits for every CTA, does no binary64 pow.  The host
+// supplies them for the step numbers it expects (cand): when t + 1 is one of
+// them they are taken as they are, with no table load and no binary64
+// division; otherwise they are computed here from the bias-correction table
+// (or pow past its end).  The host computes them with the same operations
+// from the same table entries, so either way the values are identical.
+// 1 / (scale * divisor): for a power-of-two scale 2^e it is (1 / divisor)
+// * 2^-e, and scaling by a power of two is exact, so the host's rounded
+// 1 / divisor scaled by 2^-e is the correctly rounded quotient itself.
 static __device__ __noinline__ void precompute_scalars(const Pass1Args& a) {
   PreScalars p;
   const RankState st = a.ranks[a.rank];
   p.t = st.t + 1;
-  if (a.bc_table && p.t <= kBcSteps) {
+  const int64_t j = a.cand_t0 - p.t;
+  if (j >= 0 && j < a.ncand) {
+    p.step_size = a.cand[j][0];
+    p.isb2 = a.cand[j][1];
+    p.decay = a.cand[j][2];
+  } else if (a.bc_table && p.t <= kBcSteps) {
     const double* bc = a.bc_table + 2 * (p.t - 1);
     step_scalars_bc(a.hp, p.t, bc[0], bc[1], &p.step_size, &p.isb2, &p.decay);
   } else {
     step_scalars(a.hp, p.t, &p.step_size, &p.isb2, &p.decay);
   }
   p.pad_ = 0;
-  p.inv = 1.0 / ((double)st.scale * a.hp.divisor);
+  const uint32_t sb = __float_as_uint(st.scale);
+  const uint32_t ex = (sb >> 23) & 0xffu;
+  if ((sb & 0x807fffffu) == 0u && ex != 0u && ex != 0xffu)
+    p.inv = scalbn(a.inv_d, 127 - (int)ex);   // scale = 2^(ex - 127)
+  else
+    p.inv = 1.0 / ((double)st.scale * a.hp.divisor);
   a.ws->pre = p;
 }
 
@@ -929,9 +947,17 @@ __global__ void __launch_bounds__(kThreads, bulk_min_ctas(CT))
           if (tile >= a.ntiles) break;
           cur.seek(a.segs, a.nseg, tile);
           const int64_t base = (tile - cur.s.tile0) * kTile;
-          if (cur.s.vec && base + kTile <= cur.s.n) {
+          // per thread, as in pass 2: a thread whose eight elements are all
+          // in the run loads them with one 16-byte access (the accumulation
+          // of their raw 16-bit values is bit-identical to the element-wise
+          // one), a thread past the end adds nothing (its sums would be +0),
+          // and only a thread that straddles the end goes element by element
+          const int64_t e0 = base + tid * kVec;
+          if (cur.s.vec && e0 + kVec <= cur.s.n) {
             acc.add_raw16<GT>(__ldcg(reinterpret_cast<const uint4*>(
-                grad_ptr(a.gptrs, cur.s, 0) + base + tid * kVec)));
+                grad_ptr(a.gptrs, cur.s, 0) + e0)));
+          } else if (cur.s.vec && e0 >= cur.s.n) {
+            // nothing in range
           } else {
             const Sums8 x = pass1_elementwise_sums<GT, false>(a, cur.s.n, cur.s.stash_off,
                                                               cur.s.gbase, cur.s.vec, base);

@@ -188,6 +188,12 @@ struct zero_opt_handle {
   zo::Workspace* ws = nullptr;
   zo::RankState* ranks = nullptr;
   double* bc_table = nullptr;  // device bias corrections of steps 1..kBcSteps
+  std::vector<double> bc_host;   // the same table, read back once at creation
+  // Adam step counter of each rank as the host expects it: advanced by every
+  // stepping launch as if it applies, and set exactly whenever a call reads or
+  // writes the rank's scaler state.  A skipped step the host has not seen
+  // leaves it ahead of the device; the scalar candidates cover seven of those.
+  std::vector<int64_t> t_mirror;
   void* pinned = nullptr;  // page-locked staging for small reads
   int64_t launches = 0;
   uint64_t clock = 0;
@@ -604,6 +610,26 @@ zero_status run(zero_opt_t h, int32_t rank, const std::vector<HostRun>& runs, in
     a1.keep_tile0 = std::max<int64_t>(0, plan->ntiles - keep);
   }
 
+  // The update scalars of the step numbers this rank's step can have: the one
+  // the host expects (its mirror + 1) and the seven below it (steps skipped
+  // since the host last read the rank's state).  Computed here in binary64
+  // exactly as the device would, from the device's own bias-correction table,
+  // so that pass 1's scalar CTA only picks the one that applies.
+  a1.inv_d = 1.0 / divisor;
+  if (mode != zo::kStatsOnly) {
+    const int64_t t_pred = h->t_mirror[rank] + 1;
+    if (t_pred >= 1 && t_pred <= zo::kBcSteps) {
+      a1.cand_t0 = t_pred;
+      a1.ncand = (int32_t)std::min<int64_t>(zo::kScalarCands, t_pred);
+      for (int j = 0; j < a1.ncand; ++j) {
+        const int64_t t = t_pred - j;
+        zo::step_scalars_bc(a1.hp, t, h->bc_host[2 * (t - 1)], h->bc_host[2 * (t - 1) + 1],
+                            &a1.cand[j][0], &a1.cand[j][1], &a1.cand[j][2]);
+      }
+    }
+    h->t_mirror[rank] = t_pred;
+  }
+
   const void* f1 = reinterpret_cast<const void*>(
       pick_pass1(h->cfg.grad_dtype, use_stash != nullptr, nbuf == 1, plan->ntiles));
   // Every step launch gets one extra CTA that computes the next step's update
@@ -844,6 +870,13 @@ zero_status zero_opt_create(const zero_opt_config* cfg, zero_opt_t* out) {
     // ready before any stream, blocking or not, can use the handle
     if (e == cudaSuccess) e = cudaStreamSynchronize(nullptr);
   }
+  if (e == cudaSuccess) {
+    // the host computes the update scalars it supplies from these very values
+    h->bc_host.resize(2 * (size_t)zo::kBcSteps);
+    e = cudaMemcpy(h->bc_host.data(), h->bc_table, sizeof(double) * 2 * zo::kBcSteps,
+                   cudaMemcpyDeviceToHost);
+  }
+  h->t_mirror.assign((size_t)cfg->world, 0);
   if (e != cudaSuccess) {
     for (cudaEvent_t ev : h->table_ev)
       if (ev) cudaEventDestroy(ev);
@@ -1053,7 +1086,9 @@ zero_status zero_opt_loss_scale(zero_opt_t h, int32_t rank, void* stream,
   if (!out) return fail(ZERO_EINVAL, "out is NULL");
   st = check_device(h);
   if (st != ZERO_OK) return st;
-  return read_small(h, &h->ranks[rank], sizeof(zo::RankState), stream, out);
+  st = read_small(h, &h->ranks[rank], sizeof(zo::RankState), stream, out);
+  if (st == ZERO_OK) h->t_mirror[rank] = out->t;
+  return st;
 }
 
 zero_status zero_opt_set_loss_scale(zero_opt_t h, int32_t rank, void* stream,
@@ -1071,6 +1106,7 @@ zero_status zero_opt_set_loss_scale(zero_opt_t h, int32_t rank, void* stream,
   cudaError_t e = cudaMemcpyAsync(&h->ranks[rank], in, sizeof(zo::RankState),
                                   cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync");
+  h->t_mirror[rank] = in->t;
   return ZERO_OK;
 }
 

@@ -71,6 +71,11 @@ struct PreScalars {
 // device at creation with the same pow as the decision's fallback).
 constexpr int64_t kBcSteps = 1 << 16;
 
+// Update scalars the host supplies with each stepping launch: those of Adam
+// steps cand_t0, cand_t0 - 1, ..., cand_t0 - (kScalarCands - 1) (the step the
+// host expects, and the ones after up to seven skipped steps it has not seen).
+constexpr int kScalarCands = 8;
+
 struct Workspace {
   unsigned int ticket;   // CTAs of pass 1 that finished; reset by the last
   int32_t fault;         // set by a CTA whose bounded wait expired; reset by decide
@@ -121,6 +126,11 @@ struct Pass1Args {
   int32_t pad3;
   int64_t keep_tile0;          // single-buffer chunks from this tile on are read
                                // with an L2 evict_last policy (ntiles: none)
+  double inv_d;                // 1 / divisor, rounded once (binary64)
+  int64_t cand_t0;             // the scalar candidates' first step (see above)
+  int32_t ncand;               // candidates supplied (0: none)
+  int32_t pad5;
+  float cand[kScalarCands][3]; // step_size, isb2, decay of step cand_t0 - j
 };
 
 struct Pass2Args {
