@@ -14,8 +14,9 @@ Fast2Sum is used where its condition does not hold: that error is about
 1e-10 on these inputs.
 
 Shapes: 3,000,017 elements (chunks of 4 tiles, a ragged tail reduced from
-global memory) in bf16 and fp16, and 409,600,013 bf16 elements (200,001
-tiles: chunks of 8).  In the bf16 cases every millionth value is also pushed
+global memory) in bf16 and fp16, 409,600,013 bf16 elements (200,001
+tiles: chunks of 8), and 1,000,003 elements in bf16 and fp16 (a grid
+short of one chunk per CTA, with a thread straddling the end of the run).  In the bf16 cases every millionth value is also pushed
 above 2^50, out of the binary32 fast range, so that its block takes the
 binary64 path.
 """
@@ -72,8 +73,9 @@ def _oracle_sumsq(g, code):
 
 
 @pytest.mark.parametrize("code,n,span", [(O.BF16, 3_000_017, 20), (O.FP16, 3_000_017, 8),
-                                         (O.BF16, 409_600_013, 20)],
-                         ids=["bf16-3M", "fp16-3M", "bf16-410M"])
+                                         (O.BF16, 409_600_013, 20),
+                                         (O.BF16, 1_000_003, 20), (O.FP16, 1_000_003, 8)],
+                         ids=["bf16-3M", "fp16-3M", "bf16-410M", "bf16-1M", "fp16-1M"])
 def test_sumsq_wide_range(code, n, span):
     import torch
 
