@@ -56,7 +56,7 @@ def test_config_default_is_the_ds_config(z):
     ("weight_decay", -0.5, 1), ("init_scale", 0.0, 1), ("min_scale", -1.0, 1),
     ("scale_factor", 0.5, 1), ("scale_window", 0, 1), ("bias_correction", 2, 1),
     ("hysteresis", 0, 1), ("max_grad_norm", float("nan"), 1), ("warmup_num_steps", -1, 1),
-    ("warmup_max_lr", -1e-3, 1),
+    ("warmup_max_lr", -1e-3, 1), ("table_kib", -1, 1), ("table_kib", (1 << 20) + 1, 1),
 ])
 def test_create_rejects_bad_config(z, field, value, status):
     cfg = z.make_config(numel=100, world=2)
@@ -179,3 +179,14 @@ def test_set_lr_validation(z, handle):
     z.zero_opt_set_lr(handle, 1e-4)
     with pytest.raises(z.ZeroOptError):
         z.zero_opt_set_lr(handle, -1.0)
+
+
+def test_counters_of_a_fresh_handle(z, handle):
+    """zero_opt_get_counters: nothing launched, uploaded or allocated after
+    creation; NULL arguments are rejected."""
+    c = z.zero_opt_get_counters(handle)
+    assert c.as_dict() == {"launches": 0, "table_uploads": 0, "table_waits": 0,
+                           "device_allocs": 0, "device_frees": 0, "tables_cached": 0,
+                           "tables_pinned": 0, "table_bytes": c.table_bytes}
+    assert z.lib().zero_opt_get_counters(None, ctypes.byref(c)) == z.ZERO_EINVAL
+    assert z.lib().zero_opt_get_counters(handle, None) == z.ZERO_EINVAL
