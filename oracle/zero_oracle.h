@@ -35,7 +35,10 @@
  * pinned to its reading, not to the pages): the hysteresis rule of
  * orc_decide (the scale falls on the hysteresis-th overflow since it last
  * changed), the linear shape of WarmupLR in orc_decide (its endpoints and
- * update counting are the pages'), and low-precision master weights in
+ * update counting are the pages'; the shape follows the linear warm-up of the
+ * script the tutorial migrates from, get_linear_schedule_with_warmup in
+ * [CSDN] §3.3, since the WarmupLR block itself gives no curve), and
+ * low-precision master weights in
  * orc_update (master == NULL: the 16-bit copy is the master, [JWZ] §1.7).
  */
 #ifndef ZERO_ORACLE_H
