@@ -40,9 +40,12 @@
 #endif
 
 // Pass 2 of a shard of at least ZO_L1_MIN_TILES tiles prefers the largest L1
-// (shared-memory carveout 0); smaller shards leave the driver's choice.
+// (shared-memory carveout 0); smaller shards get ZO_SMALL_CARVEOUT percent.
 #ifndef ZO_L1_MIN_TILES
 #define ZO_L1_MIN_TILES 1024
+#endif
+#ifndef ZO_SMALL_CARVEOUT
+#define ZO_SMALL_CARVEOUT 58
 #endif
 #include "zero_opt.h"
 
@@ -531,15 +534,18 @@ Pass2Fn pick_pass2(int gdt, int pdt, int src, bool m16) {
 
 // Pass 2's shared-memory carveout preference for a shard of `ntiles` tiles.
 // On large shards the largest L1 measured 10.42 -> 10.34 ms per step on the
-// 2.27B-parameter list and 4.559 -> 4.535 ms on the 1B-parameter shard; on a
+// 2.27B-parameter list and 4.559 -> 4.535 ms on the 1B-parameter shard.  On a
 // 1M-parameter shard (489 tiles) it cost 14.1 -> 18.6 us, since the pass-2
-// CTAs then cannot wait on the SMs pass 1 still holds.  The attribute belongs
-// to the kernel function (process-wide), so it is set only when the wanted
-// value changes; a stale value costs time, never correctness.
+// CTAs then cannot wait on the SMs pass 1 still holds; left to the driver's
+// choice the same step took 14.1, 15.5, 16.2 or 18.2 us from one process to
+// the next, while 58% (room for the four resident pass-1 CTAs of a small
+// shard) gave 14.33 us in every process.  The attribute belongs to the kernel
+// function (process-wide), so it is set on first use and again only when the
+// wanted value changes; a stale value costs time, never correctness.
 void prefer_l1(const void* fn, int64_t ntiles) {
   static std::mutex mu;
   static std::vector<std::pair<const void*, int>> set;
-  const int want = ntiles >= ZO_L1_MIN_TILES ? 0 : -1;   // -1: the driver's choice
+  const int want = ntiles >= ZO_L1_MIN_TILES ? 0 : ZO_SMALL_CARVEOUT;
   std::lock_guard<std::mutex> lock(mu);
   for (auto& kv : set) {
     if (kv.first == fn) {
@@ -550,8 +556,7 @@ void prefer_l1(const void* fn, int64_t ntiles) {
       return;
     }
   }
-  if (want != -1 &&
-      cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, want) != cudaSuccess)
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, want) != cudaSuccess)
     return;
   set.emplace_back(fn, want);
 }
