@@ -292,6 +292,19 @@ __device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
   return d;
 }
 
+// (hi, lo) + (hi, lo) in binary32 operations: TwoSum of the high parts, the
+// low parts added to its error, renormalised by Fast2Sum (Dekker).  Used on
+// non-negative sums of squares, where the renormalisation's condition
+// |s| >= |e| holds; the result carries about 44 significant bits.
+__device__ __forceinline__ float2 add22(float2 a, float2 b) {
+  const float s = __fadd_rn(a.x, b.x);
+  const float bp = __fsub_rn(s, a.x);
+  float e = __fadd_rn(__fsub_rn(a.x, __fsub_rn(s, bp)), __fsub_rn(b.x, bp));
+  e = __fadd_rn(e, __fadd_rn(a.y, b.y));
+  const float hi = __fadd_rn(s, e);
+  return make_float2(hi, __fsub_rn(e, __fsub_rn(hi, s)));
+}
+
 struct SqAcc {
 #if ZO_PACKED_SQ
   f32x2 H = 0ull, L = 0ull;    // lane 0 and lane 1 in one register each
@@ -481,7 +494,43 @@ struct SqAcc {
 #endif
     return __dadd_rn(__dadd_rn(a, b), slow);
   }
+  // The same sum without the binary64 part, in binary32 pairs (add22), for a
+  // CTA none of whose threads took the binary64 path (slow == 0).
+  __device__ __forceinline__ float2 total_ff() const {
+#if ZO_PACKED_SQ
+    const float2 a = add22(make_float2(f2_lo(H), f2_lo(L)), make_float2(f2_hi(H), f2_hi(L)));
+    const float2 b = add22(make_float2(f2_lo(H2), f2_lo(L2)), make_float2(f2_hi(H2), f2_hi(L2)));
+    return add22(a, b);
+#else
+    return add22(make_float2(hi0, lo0), make_float2(hi1, lo1));
+#endif
+  }
 };
+
+// Fixed-shape CTA sum of binary32 pairs (add22), rounded once to binary64 in
+// thread 0 (where it is valid): the hi + lo of one pair is exact there.  The
+// same tree as block_sum at binary32 speed; GB300's binary64 rate is a small
+// fraction of its binary32 rate, and this sum sits on every step's serial
+// path.
+__device__ __forceinline__ double block_sum_ff(float2 v, float2* red) {
+  __syncthreads();
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float2 o = make_float2(__shfl_down_sync(0xffffffffu, v.x, off),
+                                 __shfl_down_sync(0xffffffffu, v.y, off));
+    v = add22(v, o);
+  }
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  double t = 0.0;
+  if (threadIdx.x == 0) {
+    float2 w = red[0];
+#pragma unroll
+    for (int k = 1; k < kThreads / 32; ++k) w = add22(w, red[k]);
+    t = __dadd_rn((double)w.x, (double)w.y);
+  }
+  return t;
+}
 
 // Fixed-shape CTA sum in binary64: the result (valid in thread 0) depends only
 // on the inputs, never on timing.
@@ -660,10 +709,14 @@ constexpr int kFoldWarpMax = 128;
 // The epilogue shared by both pass-1 kernels: one binary64 partial and one
 // overflow flag per CTA; the CTA that finishes last folds them in a fixed
 // order and takes the decisions.
-__device__ __forceinline__ void pass1_finish(const Pass1Args& a, double mine, int flag,
+__device__ __forceinline__ void pass1_finish(const Pass1Args& a, const SqAcc& acc, int flag,
                                              double* red, int* s_last) {
   const int tid = threadIdx.x;
-  const double blk = block_sum(mine, red);
+  // the CTA's partial: in binary32 pairs unless a thread holds binary64 sums
+  // (values outside the range whose squares binary32 holds exactly)
+  const int slow = __syncthreads_or(acc.slow != 0.0);
+  const double blk = slow ? block_sum(acc.total(), red)
+                          : block_sum_ff(acc.total_ff(), reinterpret_cast<float2*>(red));
   const int any = __syncthreads_or(flag);
   if (tid == 0) {
     a.ws->part_sumsq[blockIdx.x] = blk;
@@ -809,7 +862,7 @@ __global__ void __launch_bounds__(kThreads, ZO_PASS1_MIN_CTAS)
       }
     }
   }
-  pass1_finish(a, acc.total(), acc.overflowed<GT>() ? 1 : 0, red, &s_last);
+  pass1_finish(a, acc, acc.overflowed<GT>() ? 1 : 0, red, &s_last);
 }
 
 // ------------------------------------------------------------- bulk copies
@@ -1014,7 +1067,7 @@ __global__ void __launch_bounds__(kThreads, bulk_min_ctas(CT))
       ++issued;
     }
   }
-  pass1_finish(a, acc.total(), acc.overflowed<GT>() ? 1 : 0, red, &s_last);
+  pass1_finish(a, acc, acc.overflowed<GT>() ? 1 : 0, red, &s_last);
 }
 
 // Any number of gradient buffers, loaded in batches of eight per tile, summed
@@ -1066,7 +1119,7 @@ __global__ void __launch_bounds__(kThreads, ZO_MULTI_MIN_CTAS)
     }
     acc.add<false>(x);
   }
-  pass1_finish(a, acc.total(), acc.overflowed<GT>() ? 1 : 0, red, &s_last);
+  pass1_finish(a, acc, acc.overflowed<GT>() ? 1 : 0, red, &s_last);
 }
 
 // ------------------------------------------------------------- pass 2
