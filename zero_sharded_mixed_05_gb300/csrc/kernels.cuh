@@ -1184,20 +1184,13 @@ __global__ void __launch_bounds__(kThreads, (M16 && SRC != 0) ? ZO_PASS2_M16_MIN
     }
   }
   pdl_wait();
+  // The decision, the first tile's run and the first tile's data are loaded
+  // together: nothing of a tile depends on the decision, so the skip test
+  // waits until those loads are in flight (on a skipped step their values are
+  // dropped and nothing is stored).  Three dependent L2 round trips become
+  // one on the path from pass 1's decision to pass 2's first update.
   const Decision* dp = a.dec;
-  if (dp->skip) {
-    // nothing is updated; the gradient lines pass 1 kept in L2 go back to
-    // evict_normal all the same (one lane per 128-byte line)
-    if (SRC == 1 && a.keep_tile0 < a.ntiles && (threadIdx.x & 7) == 0) {
-      RunCursor cur;
-      for (int64_t tile = a.keep_tile0 + blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
-        cur.seek(a.segs, a.nseg, tile);
-        const int64_t e0 = (tile - cur.s.tile0) * kTile + threadIdx.x * kVec;
-        if (cur.s.vec && e0 + kVec <= cur.s.n) l2_normal(grad_ptr(a.gptrs, cur.s, 0) + e0);
-      }
-    }
-    return;
-  }
+  const int skip = dp->skip;
   Scalars c;
   c.coef = dp->coef;
   c.b1 = dp->b1;
@@ -1210,8 +1203,7 @@ __global__ void __launch_bounds__(kThreads, (M16 && SRC != 0) ? ZO_PASS2_M16_MIN
   c.step_size = dp->step_size;
   const int tid = threadIdx.x;
   const int64_t G = gridDim.x;
-  if ((int64_t)blockIdx.x >= a.ntiles) return;
-  const int64_t cnt = (a.ntiles - 1 - blockIdx.x) / G + 1;
+  const int64_t cnt = (int64_t)blockIdx.x < a.ntiles ? (a.ntiles - 1 - blockIdx.x) / G + 1 : 0;
   RunCursor cur;
   for (int64_t k = cnt - 1; k >= 0; --k) {
     const int64_t tile = blockIdx.x + k * G;
@@ -1221,16 +1213,15 @@ __global__ void __launch_bounds__(kThreads, (M16 && SRC != 0) ? ZO_PASS2_M16_MIN
     const int64_t e0 = base + tid * kVec;
     if (s.vec && e0 + kVec <= s.n) {
       float x[kVec], p[kVec], m[kVec], v[kVec];
+      const unsigned short* gp = nullptr;
+      uint4 graw = make_uint4(0u, 0u, 0u, 0u);
       if (SRC == -1) {
         const float4* st = reinterpret_cast<const float4*>(a.stash + s.stash_off + e0);
         f4_to(__ldcs(st), x);
         f4_to(__ldcs(st + 1), x + 4);
       } else if (SRC == 1) {
-        const unsigned short* gp = grad_ptr(a.gptrs, s, 0) + e0;
-        Fmt<GT>::dec8(__ldcs(reinterpret_cast<const uint4*>(gp)), x);
-        if (tile >= a.keep_tile0 && (tid & 7) == 0) l2_normal(gp);
-#pragma unroll
-        for (int i = 0; i < kVec; ++i) x[i] = __fadd_rn(0.0f, x[i]);
+        gp = grad_ptr(a.gptrs, s, 0) + e0;
+        graw = __ldcs(reinterpret_cast<const uint4*>(gp));   // decoded below
       } else {
 #pragma unroll
         for (int i = 0; i < kVec; ++i) x[i] = 0.0f;
@@ -1277,6 +1268,16 @@ __global__ void __launch_bounds__(kThreads, (M16 && SRC != 0) ? ZO_PASS2_M16_MIN
         f4_to(__ldcs(vm), v);
         f4_to(__ldcs(vm + 1), v + 4);
       }
+      // every load of the tile is issued above this point; the decision is
+      // used below it
+      asm volatile("" ::: "memory");
+      if (skip) break;
+      if (SRC == 1) {
+        Fmt<GT>::dec8(graw, x);
+        if (tile >= a.keep_tile0 && (tid & 7) == 0) l2_normal(gp);
+#pragma unroll
+        for (int i = 0; i < kVec; ++i) x[i] = __fadd_rn(0.0f, x[i]);
+      }
 #pragma unroll
       for (int i = 0; i < kVec; ++i) adam_elem(x[i], p[i], m[i], v[i], c);
       if (w8) {
@@ -1298,6 +1299,7 @@ __global__ void __launch_bounds__(kThreads, (M16 && SRC != 0) ? ZO_PASS2_M16_MIN
       }
       __stcs(reinterpret_cast<uint4*>(p16), Fmt<PT>::enc8(p));
     } else {
+      if (skip) break;
 #pragma unroll
       for (int i = 0; i < kVec; ++i) {
         const int64_t e = s.vec ? e0 + i : base + (int64_t)i * kThreads + tid;
@@ -1318,6 +1320,18 @@ __global__ void __launch_bounds__(kThreads, (M16 && SRC != 0) ? ZO_PASS2_M16_MIN
         __stcs(s.m + e, m);
         __stcs(s.v + e, v);
         *p16 = Fmt<PT>::enc(p);
+      }
+    }
+  }
+  if (skip) {
+    // nothing was updated; the gradient lines pass 1 kept in L2 go back to
+    // evict_normal all the same (one lane per 128-byte line)
+    if (SRC == 1 && a.keep_tile0 < a.ntiles && (tid & 7) == 0) {
+      RunCursor kc;
+      for (int64_t tile = a.keep_tile0 + blockIdx.x; tile < a.ntiles; tile += G) {
+        kc.seek(a.segs, a.nseg, tile);
+        const int64_t e0 = (tile - kc.s.tile0) * kTile + tid * kVec;
+        if (kc.s.vec && e0 + kVec <= kc.s.n) l2_normal(grad_ptr(a.gptrs, kc.s, 0) + e0);
       }
     }
   }
