@@ -106,21 +106,26 @@ ZO_HD inline Decision decide_core(const Hyper& hp, RankState& st, double sumsq, 
     st.last_skipped = 1;
   } else {
     const double norm = sqrt(sumsq) * inv;
+    // clip = min(1, max_norm / b) with b = norm + 1e-6.  For binary64
+    // max_norm >= b the rounded quotient is at least 1; for max_norm < b the
+    // exact quotient is at most 1 - 2^-53 (max_norm is at most b less one
+    // unit in b's last place), so it rounds below 1.  The division is
+    // therefore needed only in the second case, and gives the same clip.
     double clip = 1.0;
-    if (hp.max_norm > 0.0) {
-      clip = hp.max_norm / (norm + 1e-6);
-      if (clip > 1.0) clip = 1.0;
+    if (hp.clip_on) {
+      const double b = norm + 1e-6;
+      if (hp.max_norm < b) clip = hp.max_norm / b;
     }
     d.skip = 0;
     d.norm = norm;
     d.coef = (float)(inv * clip);
     st.t += 1;
     scalars(st.t, &d.step_size, &d.isb2, &d.decay);
-    d.b1 = (float)hp.beta1;
-    d.omb1 = (float)(1.0 - hp.beta1);
-    d.b2 = (float)hp.beta2;
-    d.omb2 = (float)(1.0 - hp.beta2);
-    d.eps = (float)hp.eps;
+    d.b1 = hp.b1f;
+    d.omb1 = hp.omb1f;
+    d.b2 = hp.b2f;
+    d.omb2 = hp.omb2f;
+    d.eps = hp.epsf;
     st.last_skipped = 0;
     st.clean += 1;
     if (hp.dynamic && st.clean == hp.window) {

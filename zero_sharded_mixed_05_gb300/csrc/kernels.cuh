@@ -714,7 +714,9 @@ __device__ __forceinline__ void pass1_finish(const Pass1Args& a, const SqAcc& ac
   const int tid = threadIdx.x;
   // the CTA's partial: in binary32 pairs unless a thread holds binary64 sums
   // (values outside the range whose squares binary32 holds exactly)
-  const int slow = __syncthreads_or(acc.slow != 0.0);
+  // (an integer test: slow is a sum of non-negative terms, never -0, and a
+  // binary64 comparison would hold GB300's slow binary64 pipe on every warp)
+  const int slow = __syncthreads_or(__double_as_longlong(acc.slow) != 0ll);
   const double blk = slow ? block_sum(acc.total(), red)
                           : block_sum_ff(acc.total_ff(), reinterpret_cast<float2*>(red));
   const int any = __syncthreads_or(flag);

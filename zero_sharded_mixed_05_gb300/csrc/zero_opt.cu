@@ -130,6 +130,12 @@ Hyper hyper_of(const zero_opt_config& c, double divisor) {
   hp.warmup_min_lr = c.warmup_min_lr;
   hp.warmup_max_lr = c.warmup_max_lr;
   hp.warmup_num_steps = c.warmup_num_steps;
+  hp.b1f = (float)hp.beta1;
+  hp.omb1f = (float)(1.0 - hp.beta1);
+  hp.b2f = (float)hp.beta2;
+  hp.omb2f = (float)(1.0 - hp.beta2);
+  hp.epsf = (float)hp.eps;
+  hp.clip_on = hp.max_norm > 0.0 ? 1 : 0;
   return hp;
 }
 

@@ -95,6 +95,11 @@ struct Hyper {
   int64_t hysteresis;
   double warmup_min_lr, warmup_max_lr;
   int64_t warmup_num_steps;
+  // The decision's step-independent binary32 constants, rounded once on the
+  // host from the binary64 values above (the device's binary64 rate is low):
+  // beta1, 1 - beta1, beta2, 1 - beta2, eps; clip_on = max_norm > 0.
+  float b1f, omb1f, b2f, omb2f, epsf;
+  int32_t clip_on;
 };
 
 // kStepGlobalDev: the global statistics are folded on the device from the
