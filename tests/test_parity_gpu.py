@@ -11,8 +11,8 @@ import pytest
 
 import oracle as O
 import synth
-from harness import (FlatCase, assert_flat_parity, exact_fraction, llama_like_shapes,
-                     run_flat, run_list, to_np16, ulp16_diff)
+from harness import (FlatCase, assert_flat_parity, assert_state, exact_fraction,
+                     llama_like_shapes, run_flat, run_list, to_np16, ulp16_diff)
 
 pytestmark = pytest.mark.gpu
 
@@ -521,6 +521,51 @@ def test_state_alignment_selects_the_access_width_not_the_result(master16):
     (a, ap), (b, bp) = run(0), run(4)
     assert arrs_equal(a, b, master16)
     assert torch.equal(ap.view(torch.int16), bp.view(torch.int16))
+
+
+def test_stash_alignment_selects_the_load_width_not_the_result():
+    """Pass 2 reads the binary32 stash with one 256-bit load per lane when the
+    stash is 32-byte aligned and with two 128-bit loads when it is only
+    16-byte aligned.  Three steps of six gradient buffers through the stash,
+    on both layouts, give bit-identical state, and both match the oracle."""
+    import torch
+
+    import zero_sharded_mixed_05_gb300 as z
+    dev = torch.device("cuda:0")
+    n, R, K = 200_003, 3, 2
+    cfg = z.make_config(numel=n, world=1, grad_dtype=z.FP16, lr=1e-3, weight_decay=0.01,
+                        max_grad_norm=0.5, dynamic_scale=False, init_scale=1.0)
+    p0 = synth.normal_np(0x5EED0E10, 0, 0, n, 0.02, synth.F32)
+    steps = [[synth.normal_torch(0x5EED0E10, 1 + s * R * K + b, n, 1e-3, synth.F16, device=dev)
+              for b in range(R * K)] for s in range(3)]
+
+    def run(shift):
+        master = torch.from_numpy(p0.copy()).to(dev)
+        m, v = torch.zeros(n, device=dev), torch.zeros(n, device=dev)
+        p16 = torch.zeros(n, dtype=torch.float16, device=dev)
+        # the stash `shift` floats past a 512-byte aligned allocation
+        stash = torch.zeros(n + 8, device=dev)[shift:shift + n]
+        h = z.zero_opt_create(cfg)
+        for g in steps:
+            z.zero_opt_step(h, 0, z.make_buffers(master, m, v, p16, g, n_ranks=R, n_micro=K,
+                                                 grads_shard_local=True, stash=stash))
+        torch.cuda.synchronize()
+        z.zero_opt_destroy(h)
+        return [master, m, v], p16
+
+    (a, ap), (b, bp) = run(0), run(4)
+    assert arrs_equal(a, b, False)
+    assert torch.equal(ap.view(torch.int16), bp.view(torch.int16))
+    orc = O.default()
+    hp = O.hparams(lr=1e-3, weight_decay=0.01, max_grad_norm=0.5, dynamic_scale=False)
+    sc = O.scaler(1.0)
+    ref = (p0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32), np.zeros(n, np.uint16))
+    for g in steps:
+        orc.step(hp, sc, [to_np16(x) for x in g], O.FP16, *ref, O.FP16, float(R * K))
+    assert_state("master", a[0].cpu().numpy(), ref[0])
+    assert_state("m", a[1].cpu().numpy(), ref[1])
+    assert_state("v", a[2].cpu().numpy(), ref[2])
+    assert ulp16_diff(to_np16(ap), ref[3]) <= 1
 
 
 def arrs_equal(a, b, master16):
