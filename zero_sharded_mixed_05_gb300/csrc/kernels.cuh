@@ -1,25 +1,26 @@
 // kernels.cuh -- sm_103a kernels of the per-shard mixed-precision ZeRO step.
 //
-// Pass 1 (steps a1..a4) has three forms:
+// Pass 1 (steps a1..a4) has two forms:
 //   pass1_bulk_kernel (one gradient buffer, the usual case): chunks of 4 or 8
 //     tiles are staged into shared memory by bulk copies (TMA, cp.async.bulk
 //     on an mbarrier, two stages per CTA);
 //   pass1_multi_kernel (R*K > 1 buffers): summed per element in binary32
-//     (rank-major order, starting from +0), optionally stored (the stash);
-//   pass1_single_kernel: the one-buffer form without bulk copies (built when
-//     ZO_PASS1_BULK is 0).
-//   Each accumulates the overflow flag and the exact sum of squares.  CTAs
-//   publish one partial each; the CTA that finishes last (atomic ticket, no
-//   waiting) folds the partials in CTA order in binary64, takes the per-step
-//   decisions (skip, clip coefficient, Adam scalars) and advances the rank's
-//   loss-scaler state.  One extra CTA computes the next step's binary64
-//   scalars while the others stream.  Pass 1 is a programmatic dependent
-//   launch of whatever precedes it on the stream and waits for it at its
-//   very start.
+//     (rank-major order, starting from +0), optionally stored (the stash).
+//   Each accumulates the overflow flag and the exact sum of squares (in
+//   binary32 pairs, binary64 only for values outside binary32's exact-square
+//   range).  Every CTA publishes one binary64 partial, summed in binary32
+//   pairs and rounded once; the CTA that finishes last (atomic ticket, no
+//   waiting) folds the partials in a fixed order in binary64 (one warp for
+//   grids of up to 128 CTAs), takes the per-step decisions (skip, clip
+//   coefficient, Adam scalars) and advances the rank's loss-scaler state.
+//   One extra CTA prepares the next step's update scalars while the others
+//   stream.  Pass 1 is a programmatic dependent launch of whatever precedes
+//   it on the stream and waits for it at its very start.
 // pass2_kernel (steps a5..a7): a programmatic dependent launch of pass 1; it
-//   reads the decision, and on a skip every CTA returns at once; otherwise it
-//   applies unscale x clip, AdamW on the fp32 master copy (or the widened
-//   16-bit master) and m, v, and writes the 16-bit parameter copy.
+//   loads the decision together with its first tile, and on a skip every CTA
+//   stores nothing; otherwise it applies unscale x clip, AdamW on the fp32
+//   master copy (or the widened 16-bit master) and m, v, and writes the
+//   16-bit parameter copy.
 //
 // Both passes are HBM-bandwidth bound streaming kernels.  Tiles are 2048
 // elements (256 threads x 8); a thread moves each of its streams with one
@@ -62,11 +63,6 @@
 // needs the larger register budget of three CTAs per SM.
 #ifndef ZO_MULTI_MIN_CTAS
 #define ZO_MULTI_MIN_CTAS 3
-#endif
-// Tiles whose 16-byte gradient loads pass 1 issues before reducing any of
-// them, when there is a single gradient buffer.
-#ifndef ZO_PASS1_UNROLL
-#define ZO_PASS1_UNROLL 4
 #endif
 
 namespace zo {
@@ -815,56 +811,6 @@ __device__ __noinline__ Sums8 pass1_elementwise_sums(const Pass1Args& a, int64_t
     x.v[i] = sum;
   }
   return x;
-}
-
-// Single gradient buffer (R*K = 1, never stashed).  ZO_PASS1_UNROLL tiles'
-// 16-byte loads are issued before any is reduced; reduction works on the raw
-// 16-bit words (SqAcc::add_raw16).
-template <typename GT>
-__global__ void __launch_bounds__(kThreads, ZO_PASS1_MIN_CTAS)
-    pass1_single_kernel(const Pass1Args a) {
-  pass1_prologue();
-  __shared__ double red[kThreads / 32];
-  __shared__ int s_last;
-  constexpr int U = ZO_PASS1_UNROLL;
-  const int tid = threadIdx.x;
-  const int64_t G = gridDim.x - a.scalar_cta;
-  if (is_scalar_cta(a) && tid == 0) precompute_scalars(a);
-  SqAcc acc;
-  RunCursorLite cur;
-  for (int64_t t0 = blockIdx.x; t0 < a.ntiles && blockIdx.x < G; t0 += U * G) {
-    uint4 raw[U];
-    bool fast[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t tile = t0 + u * G;
-      fast[u] = false;
-      if (tile < a.ntiles) {
-        cur.seek(a.segs, a.nseg, tile);
-        const int64_t e0 = (tile - cur.s.tile0) * kTile + tid * kVec;
-        if (cur.s.vec && e0 + kVec <= cur.s.n) {
-          raw[u] = __ldcg(reinterpret_cast<const uint4*>(grad_ptr(a.gptrs, cur.s, 0) + e0));
-          fast[u] = true;
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t tile = t0 + u * G;
-      if (tile >= a.ntiles) continue;
-      if (fast[u]) {
-        // the sum is 0 + g, which differs from g only in the sign of a zero
-        // (irrelevant to the statistics)
-        acc.add_raw16<GT>(raw[u]);
-      } else {
-        cur.seek(a.segs, a.nseg, tile);
-        const Sums8 x = pass1_elementwise_sums<GT, false>(a, cur.s.n, cur.s.stash_off, cur.s.gbase,
-                                                          cur.s.vec, (tile - cur.s.tile0) * kTile);
-        acc.add<false>(x.v);
-      }
-    }
-  }
-  pass1_finish(a, acc, acc.overflowed<GT>() ? 1 : 0, red, &s_last);
 }
 
 // ------------------------------------------------------------- bulk copies

@@ -49,10 +49,6 @@
 #endif
 #include "zero_opt.h"
 
-// 1: a single gradient buffer takes the bulk-copy pass 1 (pass1_bulk_kernel)
-#ifndef ZO_PASS1_BULK
-#define ZO_PASS1_BULK 1
-#endif
 
 namespace {
 thread_local std::string g_err;
@@ -498,21 +494,14 @@ constexpr int64_t kBigChunkTiles = 200000;
 
 Pass1Fn pick_pass1(int gdt, bool stash, bool one, int64_t ntiles) {
   // a single buffer is never stashed (the stash needs more than four)
-#if ZO_PASS1_BULK
   if (one) {
     const bool big = ntiles >= kBigChunkTiles;
     if (gdt == ZERO_FP16)
       return big ? zo::pass1_bulk_kernel<__half, 8> : zo::pass1_bulk_kernel<__half, 4>;
     return big ? zo::pass1_bulk_kernel<__nv_bfloat16, 8> : zo::pass1_bulk_kernel<__nv_bfloat16, 4>;
   }
-#else
-  (void)ntiles;
-#endif
-  if (gdt == ZERO_FP16) {
-    if (one) return zo::pass1_single_kernel<__half>;
+  if (gdt == ZERO_FP16)
     return stash ? zo::pass1_multi_kernel<__half, true> : zo::pass1_multi_kernel<__half, false>;
-  }
-  if (one) return zo::pass1_single_kernel<__nv_bfloat16>;
   return stash ? zo::pass1_multi_kernel<__nv_bfloat16, true>
                : zo::pass1_multi_kernel<__nv_bfloat16, false>;
 }
@@ -683,7 +672,7 @@ zero_status run(zero_opt_t h, int32_t rank, const std::vector<HostRun>& runs, in
   a1.scalar_cta = mode != zo::kStatsOnly ? 1 : 0;
   // work units: tiles, or the bulk kernel's chunks of 4 or 8 tiles
   int64_t units = a1.ntiles;
-  if (ZO_PASS1_BULK && nbuf == 1 && use_stash == nullptr) {
+  if (nbuf == 1 && use_stash == nullptr) {
     const int64_t ct = plan->ntiles >= kBigChunkTiles ? 8 : 4;
     units = (a1.ntiles + ct - 1) / ct;
   }
