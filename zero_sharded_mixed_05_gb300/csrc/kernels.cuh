@@ -243,7 +243,7 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
 // element.  Each square is therefore formed exactly as p + e (p = s*s rounded,
 // e = fma(s, s, -p)) and added into a per-thread double-binary32 accumulator
 // (hi, lo) with Knuth's TwoSum; even and odd elements go to two independent
-// accumulators (the two lanes of one f32x2 register pair when ZO_PACKED_SQ)
+// accumulators (the two lanes of one f32x2 register pair)
 // so consecutive additions do not wait on each other.  The thread's total
 // hi + lo is taken in binary64; the accumulated error is a few units of 2^-48
 // of the thread's sum.  Every operation is an explicit IEEE round-to-nearest
@@ -253,9 +253,6 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
 // or whose values are all nonzero and below 2^-40 (squares near underflow),
 // are summed in binary64 instead.  amax (the largest |s| bit pattern seen)
 // gives the overflow flag: inf and NaN patterns are >= 0x7f800000.
-#ifndef ZO_PACKED_SQ
-#define ZO_PACKED_SQ 1
-#endif
 
 // Two binary32 lanes in one 64-bit register, for the f32x2 instructions.  The
 // explicit .rn rounding keeps each lane an IEEE binary32 operation that the
@@ -302,40 +299,13 @@ __device__ __forceinline__ float2 add22(float2 a, float2 b) {
 }
 
 struct SqAcc {
-#if ZO_PACKED_SQ
   f32x2 H = 0ull, L = 0ull;    // lane 0 and lane 1 in one register each
   f32x2 H2 = 0ull, L2 = 0ull;  // a second pair (add_raw16_2): two dependency chains
-#else
-  float hi0 = 0.0f, lo0 = 0.0f, hi1 = 0.0f, lo1 = 0.0f;
-#endif
   double slow = 0.0;
   uint32_t amax = 0u;
 
-  static __device__ __forceinline__ void two_sum_add(float& hi, float& lo, float x) {
-    const float p = __fmul_rn(x, x);
-    const float e = __fmaf_rn(x, x, -p);
-    const float t = __fadd_rn(hi, p);
-    const float bp = __fsub_rn(t, hi);
-    const float ap = __fsub_rn(t, bp);
-    const float err = __fadd_rn(__fsub_rn(hi, ap), __fsub_rn(p, bp));
-    lo = __fadd_rn(lo, __fadd_rn(err, e));
-    hi = t;
-  }
-
-  // Square known to be exact in binary32 (a 16-bit value in the fast range):
-  // TwoSum only.
-  static __device__ __forceinline__ void two_sum_add_exact(float& hi, float& lo, float x) {
-    const float p = __fmul_rn(x, x);
-    const float t = __fadd_rn(hi, p);
-    const float bp = __fsub_rn(t, hi);
-    const float ap = __fsub_rn(t, bp);
-    lo = __fadd_rn(lo, __fadd_rn(__fsub_rn(hi, ap), __fsub_rn(p, bp)));
-    hi = t;
-  }
-
   // a to lane 0, b to lane 1.
   __device__ __forceinline__ void pair(float a, float b) {
-#if ZO_PACKED_SQ
     const f32x2 X = f2_pack(a, b);
     const f32x2 P = f2_mul(X, X);
     const f32x2 E = f2_fma(X, X, P ^ 0x8000000080000000ull);
@@ -344,12 +314,7 @@ struct SqAcc {
     const f32x2 AP = f2_sub(T, BP);
     L = f2_add(L, f2_add(f2_add(f2_sub(H, AP), f2_sub(P, BP)), E));
     H = T;
-#else
-    two_sum_add(hi0, lo0, a);
-    two_sum_add(hi1, lo1, b);
-#endif
   }
-#if ZO_PACKED_SQ
   static __device__ __forceinline__ void pair_exact_into(f32x2& H, f32x2& L, float a, float b) {
     const f32x2 X = f2_pack(a, b);
     const f32x2 P = f2_mul(X, X);
@@ -370,14 +335,8 @@ struct SqAcc {
     L = f2_add(L, f2_sub(P, f2_sub(T, H)));
     H = T;
   }
-#endif
   __device__ __forceinline__ void pair_exact(float a, float b) {
-#if ZO_PACKED_SQ
     pair_exact_into(H, L, a, b);
-#else
-    two_sum_add_exact(hi0, lo0, a);
-    two_sum_add_exact(hi1, lo1, b);
-#endif
   }
 
   // EXACT_SQ: every s is a converted 16-bit value, whose square (fp16: 22
@@ -431,7 +390,6 @@ struct SqAcc {
       slow = __dadd_rn(slow, d);
     }
   }
-#if ZO_PACKED_SQ
   // As add_raw16 for two blocks of eight, into the two accumulator pairs.
   template <typename GT>
   __device__ __forceinline__ void add_raw16_2(const uint4& r, const uint4& q) {
@@ -472,34 +430,25 @@ struct SqAcc {
       add_raw16<GT>(q);
     }
   }
-#endif
   template <typename GT>
   __device__ __forceinline__ bool overflowed() const {
     return amax >= 0x7f800000u || amax16 >= Fmt<GT>::kInf;
   }
 
   __device__ __forceinline__ double total() const {
-#if ZO_PACKED_SQ
     const float hi0 = f2_lo(H), lo0 = f2_lo(L), hi1 = f2_hi(H), lo1 = f2_hi(L);
-#endif
     double a = __dadd_rn((double)hi0, (double)lo0);
     double b = __dadd_rn((double)hi1, (double)lo1);
-#if ZO_PACKED_SQ
     a = __dadd_rn(a, __dadd_rn((double)f2_lo(H2), (double)f2_lo(L2)));
     b = __dadd_rn(b, __dadd_rn((double)f2_hi(H2), (double)f2_hi(L2)));
-#endif
     return __dadd_rn(__dadd_rn(a, b), slow);
   }
   // The same sum without the binary64 part, in binary32 pairs (add22), for a
   // CTA none of whose threads took the binary64 path (slow == 0).
   __device__ __forceinline__ float2 total_ff() const {
-#if ZO_PACKED_SQ
     const float2 a = add22(make_float2(f2_lo(H), f2_lo(L)), make_float2(f2_hi(H), f2_hi(L)));
     const float2 b = add22(make_float2(f2_lo(H2), f2_lo(L2)), make_float2(f2_hi(H2), f2_hi(L2)));
     return add22(a, b);
-#else
-    return add22(make_float2(hi0, lo0), make_float2(hi1, lo1));
-#endif
   }
 };
 
@@ -965,15 +914,10 @@ __global__ void __launch_bounds__(kThreads, bulk_min_ctas(CT))
     if (!s_err) {
       if (*reinterpret_cast<volatile int*>(&s_whole[i % S])) {
         const uint4* sb = &stage_buf[(i % S) * kChunkTiles * kThreads + tid];
-#if ZO_PACKED_SQ
         // tiles in pairs, into two accumulator chains (CT is even)
 #pragma unroll
         for (int k = 0; k < kChunkTiles; k += 2)
           acc.add_raw16_2<GT>(sb[k * kThreads], sb[(k + 1) * kThreads]);
-#else
-#pragma unroll
-        for (int k = 0; k < kChunkTiles; ++k) acc.add_raw16<GT>(sb[k * kThreads]);
-#endif
       } else {
         RunCursorLite cur;
         for (int k = 0; k < kChunkTiles; ++k) {

@@ -33,11 +33,6 @@
 #define ZO_L2_KEEP_BYTES (64ll << 20)
 #endif
 
-// Preferred shared-memory carveout (percent) set on every kernel; -1 leaves
-// the driver's choice.
-#ifndef ZO_SMEM_CARVEOUT
-#define ZO_SMEM_CARVEOUT -1
-#endif
 
 // Pass 2 of a shard of at least ZO_L1_MIN_TILES tiles prefers the largest L1
 // (shared-memory carveout 0); smaller shards get ZO_SMALL_CARVEOUT percent.
@@ -280,11 +275,6 @@ int occupancy(zero_opt_t h, const void* fn) {
   const size_t smem = dyn_smem(fn);
   if (smem > 0)
     cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-#if ZO_SMEM_CARVEOUT >= 0
-  // one shared-memory carveout for every kernel, so that consecutive
-  // launches never wait for an SM to change its L1/shared split
-  cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, ZO_SMEM_CARVEOUT);
-#endif
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, zo::kThreads, smem) != cudaSuccess ||
       n < 1)
