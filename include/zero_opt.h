@@ -525,8 +525,10 @@ zero_status zero_opt_grad_stats_noalloc(const void* const* grads, int32_t n_bufs
  * machine without a GPU.  The results are those of zero_opt_step on the same
  * inputs: the same binary32 operation sequence per element, the same 16-bit
  * rounding, the same decisions (one shared implementation) and the same loss
- * scale sequence; only the sum of squares may differ from the device's in the
- * last bits of its binary64 value (both are compensated sums).
+ * scale sequence; only the sum of squares may differ from the device's, by
+ * about 1e-13 relative or less (both are compensated sums, added in different
+ * orders), and through the clip coefficient that can move the clipped
+ * steps' results by a unit in their last place.
  *
  * zero_host_create: `n_threads` worker threads (<= 0: the number of hardware
  * threads; at most 1024), started here and kept until zero_host_destroy.
