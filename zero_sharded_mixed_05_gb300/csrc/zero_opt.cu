@@ -526,24 +526,30 @@ Pass2Fn pick_pass2(int gdt, int pdt, int src, bool m16) {
 // the next, while 58% (room for the four resident pass-1 CTAs of a small
 // shard) gave 14.33 us in every process.  The attribute belongs to the kernel
 // function (process-wide), so it is set on first use and again only when the
-// wanted value changes; a stale value costs time, never correctness.
-void prefer_l1(const void* fn, int64_t ntiles) {
+// wanted value changes (per device: the attribute is set in the current
+// device's context); a stale value costs time, never correctness.
+void prefer_l1(int device, const void* fn, int64_t ntiles) {
+  struct Entry {
+    int device;
+    const void* fn;
+    int value;
+  };
   static std::mutex mu;
-  static std::vector<std::pair<const void*, int>> set;
+  static std::vector<Entry> set;
   const int want = ntiles >= ZO_L1_MIN_TILES ? 0 : ZO_SMALL_CARVEOUT;
   std::lock_guard<std::mutex> lock(mu);
-  for (auto& kv : set) {
-    if (kv.first == fn) {
-      if (kv.second != want &&
+  for (Entry& e : set) {
+    if (e.device == device && e.fn == fn) {
+      if (e.value != want &&
           cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, want) ==
               cudaSuccess)
-        kv.second = want;
+        e.value = want;
       return;
     }
   }
   if (cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, want) != cudaSuccess)
     return;
-  set.emplace_back(fn, want);
+  set.push_back({device, fn, want});
 }
 
 // `dependent`: launched as a programmatic dependent of the previous kernel on
@@ -692,7 +698,7 @@ zero_status run(zero_opt_t h, int32_t rank, const std::vector<HostRun>& runs, in
       pick_pass2(h->cfg.grad_dtype, h->cfg.param_dtype, src, h->cfg.master16 != 0));
   int64_t g2 = (int64_t)occupancy(h, f2) * h->sms;
   g2 = std::min<int64_t>(g2, plan->ntiles);
-  prefer_l1(f2, plan->ntiles);
+  prefer_l1(h->device, f2, plan->ntiles);
   // with the timing hook an event sits between the passes, and pass 2 is
   // an ordinary launch
   st = launch_kernel(h, f2, (int)g2, &a2, stream, h->ev[1] == nullptr);
