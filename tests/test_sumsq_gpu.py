@@ -5,9 +5,11 @@ Pass 1 squares each converted 16-bit gradient exactly in binary32 and adds the
 squares into pairs of binary32 words per thread. The addition is TwoSum, or
 Fast2Sum where the kernel has shown that the running sum is at least every
 square of the block. Both are error-free, and their error terms are equal.
-The pairs are then folded in binary64 in a fixed order.  The total is
-therefore within a few units of 2^-48 of the exact sum. The oracle computes
-it to within one binary64 rounding.  On gradients whose magnitudes span about
+Each CTA then sums its threads' pairs in binary32-pair arithmetic and rounds
+the result once to binary64 (in binary64 throughout when one of its values
+took the binary64 path), and the CTAs' partials are folded in binary64 in a
+fixed order.  The total is therefore within about 1e-13 of the exact sum,
+relative. The oracle computes it to within one binary64 rounding.  On gradients whose magnitudes span about
 2^±20 the two must agree to 5e-12 relative. That is seven orders tighter
 than the 1e-5 of the parity tests. It is also tight enough to fail if
 Fast2Sum is used where its condition does not hold: that error is about
@@ -18,7 +20,8 @@ global memory) in bf16 and fp16, 409,600,013 bf16 elements (200,001
 tiles: chunks of 8), and 1,000,003 elements in bf16 and fp16 (a grid
 short of one chunk per CTA, with a thread straddling the end of the run).  In the bf16 cases every millionth value is also pushed
 above 2^50, out of the binary32 fast range, so that its block takes the
-binary64 path.
+binary64 path and its CTA sums its partial in binary64; the fp16 cases keep
+every CTA on the binary32-pair path.
 """
 import numpy as np
 import pytest
