@@ -12,7 +12,8 @@ Llama-3-8B ZeRO-2 shard its 100 steps under a dynamic scale of 2^16 with an
 overflow injected every 50 steps at a seeded index: those two steps are
 skipped and halve the scale, which ends at 2^14 ("DeepSpeed tutorial" §2.2,
 §3.2: skip and lower the scale on overflow; window 1000, so no growth).  The
-other workloads run three steps with an overflow on the second.
+other workloads run three steps with an overflow on the second, and so does
+a flat shard of 2,200,000,007 elements (offsets past 2^31).
 """
 import numpy as np
 import pytest
@@ -52,7 +53,7 @@ def _chunk_stats(orc, grads, code, c0, c1):
 class Run:
     """A workload as bench.Setup builds it, plus the oracle's view of a sample."""
 
-    def __init__(self, name):
+    def __init__(self, name, extra=()):
         import torch
 
         import bench
@@ -82,6 +83,9 @@ class Run:
         for gi, (master, m, v, p16, _) in enumerate(self.groups):
             n = m.numel()
             idx = _sample(n, 1000 + gi, 60_000 if len(self.groups) == 1 else 2_000)
+            if extra:
+                ex = np.asarray(extra, dtype=np.int64)
+                idx = np.unique(np.concatenate([idx, ex[(ex >= 0) & (ex < n)]]))
             ti = torch.from_numpy(idx).cuda()
             # with 16-bit masters (master None) the parameters are the state
             self.samples.append(dict(ti=ti,
@@ -128,11 +132,12 @@ class Run:
             assert ulp16_diff(to_np16(p16[ti]), smp["p16"]) <= 1
 
 
-def _run(name, steps=3, inject_steps=(2,)):
+def _run(name, steps=3, inject_steps=(2,), extra=()):
     """`steps` steps of workload `name`; on each step of `inject_steps` a +inf
-    replaces one gradient at an index drawn from the seeded generator."""
+    replaces one gradient at an index drawn from the seeded generator.
+    `extra`: element indices sampled besides the seeded ones."""
     import zero_sharded_mixed_05_gb300 as z
-    run = Run(name)
+    run = Run(name, extra)
     n0 = run.groups[0][1].numel()
     where = synth.seeded_indices(run.s.w["seed"], 99, len(inject_steps), 0, n0)
     inject_at = dict(zip(inject_steps, where))
@@ -182,3 +187,21 @@ def test_fullsize_per_tensor_list():
 
 def test_fullsize_gpt2_low_precision_master():
     _run("gpt2_master16")
+
+
+def test_fullsize_flat_shard_past_2_31_elements():
+    """The GPT-2 settings on one flat bf16 shard of 2,200,000,007 elements:
+    element offsets past 2^31 and a ragged last tile.  Three steps with an
+    overflow on the second, sampled also around elements 2^31 and at the
+    end."""
+    import bench
+    n = 2_200_000_007
+    w = dict(bench.WORKLOADS["gpt2"])
+    w["numel"] = n
+    w["desc"] = w["desc"] + f" [resized to {n:,} params]"
+    bench.WORKLOADS["flat_2200M"] = w
+    edge = [2**31 + d for d in range(-9, 10)] + [n - 9 + d for d in range(9)]
+    try:
+        _run("flat_2200M", extra=edge)
+    finally:
+        del bench.WORKLOADS["flat_2200M"]

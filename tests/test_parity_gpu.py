@@ -568,6 +568,52 @@ def test_stash_alignment_selects_the_load_width_not_the_result():
     assert ulp16_diff(to_np16(ap), ref[3]) <= 1
 
 
+@pytest.mark.parametrize("stash", [False, True], ids=["reread", "stash"])
+def test_buffer_limit_of_1024_matches_the_oracle_and_1025_is_refused(stash):
+    """R*K = 32 x 32 = 1024 gradient buffers, the most one step takes, over a
+    ragged shard of 3001 elements: three clipped steps match the oracle, with
+    the sums re-read in pass 2 and through the stash.  41 x 25 = 1025 buffers
+    are refused with ZERO_EINVAL before anything is launched."""
+    import torch
+
+    import zero_sharded_mixed_05_gb300 as z
+    dev = torch.device("cuda:0")
+    n, R, K = 3001, 32, 32
+    cfg = z.make_config(numel=n, world=1, grad_dtype=z.FP16, lr=1e-3, weight_decay=0.01,
+                        max_grad_norm=0.5, dynamic_scale=False, init_scale=1.0)
+    p0 = synth.normal_np(0x5EED0E20, 0, 0, n, 0.02, synth.F32)
+    master = torch.from_numpy(p0.copy()).to(dev)
+    m, v = torch.zeros(n, device=dev), torch.zeros(n, device=dev)
+    p16 = torch.zeros(n, dtype=torch.float16, device=dev)
+    st = torch.zeros(n, device=dev) if stash else None
+    h = z.zero_opt_create(cfg)
+    orc = O.default()
+    hp = O.hparams(lr=1e-3, weight_decay=0.01, max_grad_norm=0.5, dynamic_scale=False)
+    sc = O.scaler(1.0)
+    ref = (p0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32), np.zeros(n, np.uint16))
+    try:
+        for step in range(3):
+            g = [synth.normal_torch(0x5EED0E20, 1 + step * R * K + b, n, 1e-3, synth.F16,
+                                    device=dev) for b in range(R * K)]
+            z.zero_opt_step(h, 0, z.make_buffers(master, m, v, p16, g, n_ranks=R, n_micro=K,
+                                                 grads_shard_local=True, stash=st))
+            orc.step(hp, sc, [to_np16(x) for x in g], O.FP16, *ref, O.FP16, float(R * K))
+        torch.cuda.synchronize()
+        assert_state("master", master.cpu().numpy(), ref[0])
+        assert_state("m", m.cpu().numpy(), ref[1])
+        assert_state("v", v.cpu().numpy(), ref[2])
+        assert ulp16_diff(to_np16(p16), ref[3]) <= 1
+        launched = z.zero_opt_launch_count(h)
+        g = [torch.zeros(n, dtype=torch.float16, device=dev)] * (41 * 25)
+        with pytest.raises(z.ZeroOptError) as e:
+            z.zero_opt_step(h, 0, z.make_buffers(master, m, v, p16, g, n_ranks=41, n_micro=25,
+                                                 grads_shard_local=True, stash=st))
+        assert e.value.status == z.ZERO_EINVAL
+        assert z.zero_opt_launch_count(h) == launched
+    finally:
+        z.zero_opt_destroy(h)
+
+
 def arrs_equal(a, b, master16):
     import torch
     first = 1 if master16 else 0         # the master array is unused with 16-bit masters
