@@ -624,7 +624,7 @@ def run_ours(args):
     # gradients (into a second device buffer set) and the download of step
     # i's parameters (from one of two alternating parameter buffers) run on
     # their own streams while step i+1 computes.
-    # The host side of the box is shared, so the link-bound figure varies from
+    # The host side of the machine is shared, so the link-bound figure varies from
     # run to run: the median of three repetitions is reported, with all three.
     e2e = None
     if not args.no_e2e:

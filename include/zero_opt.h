@@ -66,7 +66,7 @@ typedef enum zero_status {
   ZERO_ERANGE = 2,   /* index or size out of range (rank >= world, ...) */
   ZERO_ENOMEM = 3,   /* host or device allocation failed in zero_opt_create */
   ZERO_ECUDA = 4,    /* a CUDA call failed, or no CUDA device is present */
-  ZERO_ENOTSUP = 5   /* option not supported by this build */
+  ZERO_ENOTSUP = 5   /* option not supported                */
 } zero_status;
 
 typedef enum zero_dtype {

@@ -107,7 +107,7 @@ def test_noalloc_stats_match_the_oracle_and_the_handle_path_on_consecutive_calls
                        _handle_path(z, grads, code, n)))
     torch.cuda.synchronize()
     # a first call sets the entry point up on this device; after it, the calls
-    # allocate nothing: neither torch's nor the driver's count of device
+    # allocate nothing: neither torch's nor the CUDA driver's count of device
     # memory moves
     _noalloc(z, inputs[0][2], inputs[0][1], inputs[0][0], out)
     used0 = torch.cuda.memory_allocated()

@@ -521,7 +521,7 @@ Pass2Fn pick_pass2(int gdt, int pdt, int src, bool m16) {
 // On large shards the largest L1 measured 10.42 -> 10.34 ms per step on the
 // 2.27B-parameter list and 4.559 -> 4.535 ms on the 1B-parameter shard.  On a
 // 1M-parameter shard (489 tiles) it cost 14.1 -> 18.6 us, since the pass-2
-// CTAs then cannot wait on the SMs pass 1 still holds; left to the driver's
+// CTAs then cannot wait on the SMs pass 1 still holds; left to the CUDA driver's
 // choice the same step took 14.1, 15.5, 16.2 or 18.2 us from one process to
 // the next, while 58% (room for the four resident pass-1 CTAs of a small
 // shard) gave 14.33 us in every process.  The attribute belongs to the kernel
